@@ -1,0 +1,229 @@
+/*
+ * fp64 CPU oracle for the selective-scan forward and the recurrent decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+ * the CPU-baseline leg of the benchmark may load this library.  It shares no
+ * code, header, table or helper with the CUDA library it is used to check.
+ *
+ * What it computes (plain definition, sequential in t, fp64 throughout):
+ *
+ *   for every batch b and channel d, with h[n] = h0[b,d,n] (or 0):
+ *     for t = 0 .. L-1:
+ *       x      = delta[b,d,t] + delta_bias[d]
+ *       Δ      = softplus(x) = log(1 + e^x)     if delta_softplus, else x
+ *       for n: h[n] = exp(Δ·A[d,n])·h[n] + Δ·B[b,n,t]·u[b,d,t]
+ *       y      = Σ_n C[b,n,t]·h[n] + D[d]·u[b,d,t]
+ *       out[b,d,t] = y · z·σ(z)  with z = z[b,d,t]   (y unchanged without z)
+ *     h_last[b,d,:] = h
+ *
+ * Sources (pages on the Mamba selective SSM):
+ *  - "Mamba状态空间模型深度解析：挑战Transformer的下一代序列建模范式" §2.1: the
+ *    selective recurrence h_k = A·h_{k-1} + B(x_k)·x_k, y_k = C(x_k)·h_k, with
+ *    B, C and Δ functions of the input; y_k reads the state after step k.
+ *  - "Mamba架构与SSM模型：高效序列建模技术解析" §2.1: zero-order-hold
+ *    Ā = exp(ΔA); §2.2: Δ = softplus(Linear(x) + param_Δ).  The Linear layer
+ *    is upstream of this operation, so its output arrives as `delta`.
+ *  - "Mamba: Linear-Time Sequence Modeling with Selective SSMs", "连续与离散SSM":
+ *    the D·u feed-through term of y = Cx + Du.
+ *  - "Mamba状态空间模型深度解析" §3.1: SiLU multiplicative gate in the block.
+ *  - "Mamba: Linear-Time Sequence Modeling with Selective SSMs", "选择性扫描要点":
+ *    the end state of one block is carried as the start ("prefix") state of
+ *    the next, which is what h0 / h_last expose.
+ *
+ * Readings where the pages leave a step open:
+ *  - B̄ is taken as Δ·B (the simplified discretisation of the input matrix),
+ *    not the exact ZOH form (ΔA)^{-1}(exp(ΔA)-I)·ΔB that §2.1 also prints.
+ *  - The gate multiplies the whole y, including the D·u term.
+ *  - softplus is the exact log(1+e^x), evaluated as max(x,0) + log1p(e^{-|x|}).
+ *  - silu(z) = z / (1 + e^{-z}).
+ *
+ * Inputs are read as the exact values of their stored type: fp32 as is, bf16
+ * (raw 16-bit patterns) widened exactly.  Results are fp64.
+ *
+ * Build: gcc -O2 -std=c11 -shared -fPIC -pthread selscan_oracle.c -lm
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* dtype codes of the input tensors u, delta, z, B, C */
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* Exact widening of one stored input element to double. */
+static double load_in(const void* p, int64_t i, int dtype) {
+  if (dtype == ORACLE_BF16) {
+    uint32_t bits = ((uint32_t)((const uint16_t*)p)[i]) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+  }
+  return (double)((const float*)p)[i];
+}
+
+static double softplus(double x) {
+  return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+typedef struct {
+  int64_t batch, dim, seqlen, dstate;
+  int in_dtype;
+  const void *u, *delta, *z, *B, *C;
+  const float *A, *D, *delta_bias, *h0;
+  const double* h0_f64; /* fp64 start state; takes precedence over h0 */
+  int delta_softplus;
+  int reverse; /* process t from L-1 down to 0 (bidirectional variant) */
+  /* rows to compute: flat indices b*dim + d; NULL = all rows */
+  const int64_t* rows;
+  int64_t nrows;
+  double* out;    /* [nrows, L] when rows != NULL, else [batch, dim, L] */
+  double* h_last; /* [nrows, N] / [batch, dim, N]; may be NULL */
+  /* work split */
+  int64_t next_row;
+  pthread_mutex_t lock;
+} fwd_job;
+
+/* The recurrence for one (b, d) row, sequential in t. */
+static void scan_row(const fwd_job* j, int64_t b, int64_t d, double* out_row, double* hl_row) {
+  const int64_t L = j->seqlen, N = j->dstate, Dm = j->dim;
+  double h[64];
+  for (int64_t n = 0; n < N; n++) {
+    const int64_t s0 = (b * Dm + d) * N + n;
+    h[n] = j->h0_f64 ? j->h0_f64[s0] : (j->h0 ? (double)j->h0[s0] : 0.0);
+  }
+  const double bias = j->delta_bias ? (double)j->delta_bias[d] : 0.0;
+  const double Dd = j->D ? (double)j->D[d] : 0.0;
+  for (int64_t s = 0; s < L; s++) {
+    const int64_t t = j->reverse ? (L - 1 - s) : s;
+    const int64_t e = (b * Dm + d) * L + t; /* element index into [B, D, L] */
+    const double u = load_in(j->u, e, j->in_dtype);
+    const double x = load_in(j->delta, e, j->in_dtype) + bias;
+    const double dt = j->delta_softplus ? softplus(x) : x;
+    double y = 0.0;
+    for (int64_t n = 0; n < N; n++) {
+      const int64_t bc = (b * N + n) * L + t; /* index into [B, N, L] */
+      const double Bv = load_in(j->B, bc, j->in_dtype);
+      const double Cv = load_in(j->C, bc, j->in_dtype);
+      const double a = (double)j->A[d * N + n];
+      const double abar = exp(dt * a);     /* Ā = exp(Δ·A) */
+      h[n] = abar * h[n] + dt * Bv * u;    /* h_t = Ā·h_{t-1} + Δ·B·u */
+      y += Cv * h[n];                      /* C·h_t reads the updated state */
+    }
+    y += Dd * u;
+    if (j->z) y *= silu(load_in(j->z, e, j->in_dtype));
+    out_row[t] = y;
+  }
+  if (hl_row)
+    for (int64_t n = 0; n < N; n++) hl_row[n] = h[n];
+}
+
+static void* fwd_worker(void* arg) {
+  fwd_job* j = (fwd_job*)arg;
+  const int64_t total = j->rows ? j->nrows : j->batch * j->dim;
+  for (;;) {
+    pthread_mutex_lock(&j->lock);
+    const int64_t r = j->next_row++;
+    pthread_mutex_unlock(&j->lock);
+    if (r >= total) break;
+    const int64_t flat = j->rows ? j->rows[r] : r;
+    const int64_t b = flat / j->dim, d = flat % j->dim;
+    scan_row(j, b, d, j->out + r * j->seqlen, j->h_last ? j->h_last + r * j->dstate : NULL);
+  }
+  return NULL;
+}
+
+/*
+ * Selective-scan forward over every row (rows == NULL) or over the listed
+ * rows only (flat b*dim + d indices; outputs are then packed per listed row).
+ * nthreads <= 1 runs on the calling thread.  Returns 0, or -1 on bad sizes.
+ */
+int oracle_selscan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype,
+                       const void* u, const void* delta, const float* A, const void* B, const void* C,
+                       const float* D, const void* z, const float* delta_bias, int delta_softplus,
+                       const float* h0, const double* h0_f64, int reverse, const int64_t* rows, int64_t nrows,
+                       double* out,
+                       double* h_last, int nthreads) {
+  if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1 || dstate > 64) return -1;
+  if (in_dtype != ORACLE_F32 && in_dtype != ORACLE_BF16) return -1;
+  if (!u || !delta || !A || !B || !C || !out) return -1;
+  fwd_job j;
+  memset(&j, 0, sizeof j);
+  j.batch = batch;
+  j.dim = dim;
+  j.seqlen = seqlen;
+  j.dstate = dstate;
+  j.in_dtype = in_dtype;
+  j.u = u;
+  j.delta = delta;
+  j.z = z;
+  j.B = B;
+  j.C = C;
+  j.A = A;
+  j.D = D;
+  j.delta_bias = delta_bias;
+  j.h0 = h0;
+  j.h0_f64 = h0_f64;
+  j.delta_softplus = delta_softplus;
+  j.reverse = reverse;
+  j.rows = rows;
+  j.nrows = nrows;
+  j.out = out;
+  j.h_last = h_last;
+  pthread_mutex_init(&j.lock, NULL);
+  if (nthreads <= 1) {
+    fwd_worker(&j);
+  } else {
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int started = 0;
+    for (int i = 0; i < nthreads; i++)
+      if (pthread_create(&th[i], NULL, fwd_worker, &j) == 0) started++;
+      else break;
+    if (started == 0) fwd_worker(&j);
+    for (int i = 0; i < started; i++) pthread_join(th[i], NULL);
+    free(th);
+  }
+  pthread_mutex_destroy(&j.lock);
+  return 0;
+}
+
+/*
+ * One recurrent decode step (the L = 1 case of the forward), in place on an
+ * fp64 state [batch, dim, dstate]: the state after the step replaces it.
+ * u, delta, z are [batch, dim]; B, C are [batch, dstate].
+ * This is the constant-memory recurrent inference mode ("Mamba架构深度剖析" §3).
+ */
+int oracle_selscan_step(int64_t batch, int64_t dim, int64_t dstate, int in_dtype, const void* u,
+                        const void* delta, const float* A, const void* B, const void* C, const float* D,
+                        const void* z, const float* delta_bias, int delta_softplus, double* state,
+                        double* out) {
+  if (batch < 0 || dim < 0 || dstate < 1 || dstate > 64) return -1;
+  if (!u || !delta || !A || !B || !C || !state || !out) return -1;
+  for (int64_t b = 0; b < batch; b++) {
+    for (int64_t d = 0; d < dim; d++) {
+      const int64_t e = b * dim + d;
+      const double uu = load_in(u, e, in_dtype);
+      const double x = load_in(delta, e, in_dtype) + (delta_bias ? (double)delta_bias[d] : 0.0);
+      const double dt = delta_softplus ? softplus(x) : x;
+      double y = 0.0;
+      for (int64_t n = 0; n < dstate; n++) {
+        double* h = &state[e * dstate + n];
+        const double Bv = load_in(B, b * dstate + n, in_dtype);
+        const double Cv = load_in(C, b * dstate + n, in_dtype);
+        *h = exp(dt * (double)A[d * dstate + n]) * (*h) + dt * Bv * uu;
+        y += Cv * (*h);
+      }
+      y += (D ? (double)D[d] : 0.0) * uu;
+      if (z) y *= silu(load_in(z, e, in_dtype));
+      out[e] = y;
+    }
+  }
+  return 0;
+}
+
+/* Scalar helpers exposed for pinning the oracle's own building blocks. */
+double oracle_softplus(double x) { return softplus(x); }
+double oracle_silu(double z) { return silu(z); }
+double oracle_load_bf16(uint16_t bits) { return load_in(&bits, 0, ORACLE_BF16); }
