@@ -1,0 +1,537 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective-scan forward (libselscan) on B300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one ``selscan_fwd`` over one batch of the workload: softplus Δ,
+discretisation, the chunked scan, the C readout, the D skip and the SiLU gate
+(every row of the forward hot path), with inputs resident in HBM.  The default
+workload is the Mamba-130M-like layer scan (batch 8, d_inner 1536, L 2048,
+d_state 16, bf16 u/δ/z/B/C, fp32 state and fp32 out).  L2 is flushed (a
+256 MiB write) before every timed step, outside the step's CUDA events.
+
+Reported: ``value`` = elements (B·D·L) per second over all GPUs, from the
+per-step CUDA-event times summed over the K timed steps (max over ranks);
+``hbm_gbs`` = algorithmic bytes / time; ``roofline`` for the fused forward
+kernel; ``e2e`` = the same metric with host (pinned) inputs copied in and the
+output copied back inside each timed step; ``cpu_baseline`` = the fp64 oracle
+on the host cores on a bounded row sample; ``decode`` = the recurrent decode
+step workload (secondary).  Under torchrun (N > 1) every rank runs its own
+shard of an N-times-larger batch (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "selective-scan elems(B·D·L)/s and HBM GB/s at 1 B300; fraction of roofline"
+DEFAULT_WORKLOAD = "mamba130m_layer"
+L2_FLUSH_BYTES = 256 << 20
+EX2_PER_CLK_PER_SM = 32  # measured on B300: ex2.approx.ftz.f32 issues 32 results / clock / SM
+FP32_PER_CLK_PER_SM = 128  # FFMA lanes per SM
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_SM_MHZ = 2032.0
+
+
+# ------------------------------------------------------------------------------------------------
+# Host-side logic (unit-tested on CPU)
+# ------------------------------------------------------------------------------------------------
+
+def measured_peaks(path=os.path.join(ROOT, "MEASURED_PEAKS.json")):
+    """(hbm GB/s, max SM MHz, source) from the generated peaks file, else the fallback."""
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("sm_max_mhz", FALLBACK_SM_MHZ)), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, FALLBACK_SM_MHZ, "fallback"
+
+
+def fwd_work(batch, dim, seqlen, dstate, in_bytes=2, out_bytes=4, h0=False, h_last=True):
+    """Algorithmic work of one selscan_fwd: elements, bytes, MUFU ops and FP32 ops.
+
+    Bytes: u, δ, z read once and out written once per element; B, C read once
+    per (b, n, t) — not per channel; A, D, Δ_bias once; h0 / h_last once.
+    MUFU: N exponentials for Ā plus 4 for softplus (exp, log) and the gate
+    (exp, reciprocal) per element.  FP32: 4 per (element, state) — Δ·A, Δu·B,
+    the state FMA, the C·h FMA — plus 8 per element.
+    """
+    elems = batch * dim * seqlen
+    nbytes = elems * (3 * in_bytes + out_bytes) + 2 * batch * dstate * seqlen * in_bytes + dim * dstate * 4 + 2 * dim * 4
+    if h0:
+        nbytes += batch * dim * dstate * 4
+    if h_last:
+        nbytes += batch * dim * dstate * 4
+    return {"elements": elems, "bytes": nbytes, "mufu": elems * (dstate + 4), "fp32": elems * (4 * dstate + 8)}
+
+
+def step_work(batch, dim, dstate, in_bytes=2, out_bytes=4):
+    """Algorithmic bytes of one decode step: state read + write, u/δ/z/out, B/C, A/D/bias."""
+    rows = batch * dim
+    return {"elements": rows,
+            "bytes": rows * (2 * dstate * 4 + 3 * in_bytes + out_bytes) + 2 * batch * dstate * in_bytes
+            + dim * dstate * 4 + 2 * dim * 4}
+
+
+def roofline_times(work, sms, hbm_gbs, sm_mhz):
+    """Seconds each resource needs at its peak: HBM bytes, MUFU ops, FP32 ops."""
+    f = sm_mhz * 1e6
+    return {"hbm": work["bytes"] / (hbm_gbs * 1e9), "mufu": work["mufu"] / (sms * EX2_PER_CLK_PER_SM * f),
+            "fp32": work["fp32"] / (sms * FP32_PER_CLK_PER_SM * f)}
+
+
+def roofline_entry(work, t_kernel, sms, hbm_gbs, sm_mhz, traffic=None):
+    """The roofline object for a forward kernel that took t_kernel seconds per launch."""
+    t = roofline_times(work, sms, hbm_gbs, sm_mhz)
+    bound = max(t, key=t.get)
+    if bound == "hbm":
+        achieved, peak, unit = work["bytes"] / t_kernel / 1e9, hbm_gbs, "GB/s"
+        kind = "hbm"
+    elif bound == "mufu":
+        achieved = work["mufu"] / t_kernel / 1e12
+        peak = sms * EX2_PER_CLK_PER_SM * sm_mhz * 1e6 / 1e12
+        unit, kind = "TFLOP/s", "alu"
+    else:
+        achieved = work["fp32"] / t_kernel / 1e12
+        peak = sms * FP32_PER_CLK_PER_SM * sm_mhz * 1e6 / 1e12
+        unit, kind = "TFLOP/s", "alu"
+    return {"bound": kind, "resource": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic,
+            "t_us": {k: v * 1e6 for k, v in t.items()}, "t_kernel_us": t_kernel * 1e6}
+
+
+def shard_batch(global_batch, rank, world):
+    """Contiguous batch range [lo, hi) of this rank (weak scaling: each rank gets global_batch / world)."""
+    per = global_batch // world
+    rem = global_batch % world
+    lo = rank * per + min(rank, rem)
+    return lo, lo + per + (1 if rank < rem else 0)
+
+
+def aggregate(elements_per_rank, seconds_per_rank):
+    """Whole-job throughput: all ranks' elements over the slowest rank's time."""
+    return sum(elements_per_rank) / max(seconds_per_rank)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_152_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload, path=os.path.join(ROOT, "profiles", "ncu_traffic.json")):
+    """DRAM bytes per launch from a committed ncu capture, if taken on the current kernel sources."""
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = rec.get(kernel, {}).get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML while the timed region runs."""
+
+    REASONS = {"hw_slowdown": "nvmlClocksEventReasonHwSlowdown",
+               "hw_thermal_slowdown": "nvmlClocksEventReasonHwThermalSlowdown",
+               "sw_thermal_slowdown": "nvmlClocksEventReasonSwThermalSlowdown",
+               "sw_power_cap": "nvmlClocksEventReasonSwPowerCap",
+               "hw_power_brake": "nvmlClocksEventReasonHwPowerBrakeSlowdown"}
+
+    def __init__(self, device_index, period_s=0.005, smi_id=None):
+        self.samples, self.reasons, self.max_mhz, self.error = [], set(), None, None
+        self.smi_id = smi_id if smi_id is not None else str(device_index)
+        self.period = period_s
+        self._stop = threading.Event()
+        self._t = None
+        try:
+            import pynvml
+
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # noqa: BLE001 - fall back to nvidia-smi polling
+            self.nv = None
+            self.error = f"{type(e).__name__}: {e}"
+        self.device_index = device_index
+        self._proc = None
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for name, const in self.REASONS.items():
+                    if r & getattr(nv, const, 0):
+                        self.reasons.add(name)
+            except Exception:  # noqa: BLE001
+                pass
+            time.sleep(self.period)
+
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+
+    def __enter__(self):
+        if self.nv is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        else:
+            import subprocess
+
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                     "-i", self.smi_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError as e:
+                self.error = (self.error or "") + f"; nvidia-smi: {e}"
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._t:
+            self._t.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate(timeout=10)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[2:6]):
+                    if v.lower() == "active":
+                        self.reasons.add(name)
+
+    def report(self):
+        r = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+             "reasons": sorted(self.reasons), "samples": len(self.samples),
+             "source": "nvml" if self.nv is not None else "nvidia-smi"}
+        if self.error:
+            r["nvml_error"] = self.error
+        return r
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+
+def _dev(torch, a, device):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def _pinned(torch, a):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    return torch.from_numpy(a).pin_memory()
+
+
+def run_ours(args, rank, world, local_rank, dist):
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    w = si.WORKLOADS[args.workload]
+    if w.steps:
+        raise SystemExit("the timed step is the forward scan; the decode workload is reported under 'decode'")
+    lo, hi = shard_batch(w.batch * world, rank, world)
+    inp = si.make_inputs(w, seed=si.BASE_SEED + si.WORKLOAD_ORDER.index(w.name) + 1000 * rank, batch=hi - lo)
+    Bsz, Dm, L, N = inp["shape"]
+    names = ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")
+    t = {k: _dev(torch, inp.get(k), device) for k in names}
+    out = torch.empty((Bsz, Dm, L), device=device, dtype=torch.float32)
+    h_last = torch.empty((Bsz, Dm, N), device=device, dtype=torch.float32) if w.returns_h_last else None
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=device, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        ss.selscan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"], delta_bias=t["delta_bias"],
+                       delta_softplus=True, h0=t["h0"], out=out, h_last=h_last, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(device)
+    smi_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local_rank)
+    with ClockSampler(local_rank, smi_id=smi_id) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            fwd()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier()
+    torch.cuda.synchronize()
+    step_s = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
+    t_sum = sum(step_s)
+    t_max = t_sum
+    if dist is not None:
+        tt = torch.tensor([t_sum], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    elems_rank = Bsz * Dm * L * args.steps
+    value = elems_rank * world / t_max
+
+    work = fwd_work(Bsz, Dm, L, N, in_bytes=2 if w.in_dtype == "bf16" else 4, out_bytes=4,
+                    h0=inp.get("h0") is not None, h_last=h_last is not None)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    hbm_gbs, sm_mhz, peak_src = measured_peaks()
+    t_kernel = t_sum / args.steps
+    roof = roofline_entry(work, t_kernel, sms, hbm_gbs, sm_mhz,
+                          traffic=recorded_traffic("selscan_fwd", args.workload))
+    roof["peak_source"] = f"{peak_src} (HBM {hbm_gbs} GB/s; SM {sm_mhz} MHz x {sms} SMs)"
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "elems/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": Bsz * world, "dim": Dm, "seqlen": L, "dstate": N,
+                   "in_dtype": w.in_dtype, "out_dtype": "f32", "state": "f32",
+                   "l2": "flushed (256 MiB write) before every timed step, outside its events"},
+        "hbm_gbs": work["bytes"] * world * args.steps / t_max / 1e9,
+        "roofline": roof,
+        "gpu_launches": args.steps,
+        "clocks": clk.report(),
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world)
+    if rank == 0 and world == 1 and not args.no_decode:
+        result["decode"] = run_decode(args, torch, ss, device, stream, flush, sms, hbm_gbs)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(inp, w, budget_cpu_s=args.cpu_budget)
+    return result
+
+
+def run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world):
+    """The same metric through the public API with pinned host buffers copied in and out each step."""
+    Bsz, Dm, L, N = inp["shape"]
+    names = ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")
+    host = {k: _pinned(torch, inp.get(k)) for k in names}
+    dev = {k: (None if host[k] is None else torch.empty_like(host[k], device=device)) for k in names}
+    out = torch.empty((Bsz, Dm, L), device=device, dtype=torch.float32)
+    out_h = torch.empty((Bsz, Dm, L), dtype=torch.float32).pin_memory()
+    hl = torch.empty((Bsz, Dm, N), device=device, dtype=torch.float32) if w.returns_h_last else None
+    hl_h = torch.empty((Bsz, Dm, N), dtype=torch.float32).pin_memory() if w.returns_h_last else None
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = out_h.numel() * 4 + (hl_h.numel() * 4 if hl_h is not None else 0)
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def one():
+        for k in names:
+            if host[k] is not None:
+                dev[k].copy_(host[k], non_blocking=True)
+        ss.selscan_fwd(dev["u"], dev["delta"], dev["A"], dev["B"], dev["C"], D=dev["D"], z=dev["z"],
+                       delta_bias=dev["delta_bias"], h0=dev["h0"], out=out, h_last=hl, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        if hl is not None:
+            hl_h.copy_(hl, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        one()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    secs = ev0.elapsed_time(ev1) / 1e3
+    if dist is not None:
+        tt = torch.tensor([secs], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        secs = float(tt.item())
+    return {"value": Bsz * Dm * L * steps * world / secs, "unit": "elems/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": secs / steps * 1e3,
+            "gpu_launches": steps}
+
+
+def run_decode(args, torch, ss, device, stream, flush, sms, hbm_gbs):
+    """Secondary: the recurrent decode workload (64 steps of selscan_step carrying the fp32 state)."""
+    w = si.WORKLOADS["decode_step"]
+    inp = si.make_inputs(w)
+    T = inp["steps"]
+    Bsz, Dm, _, N = inp["shape"]
+    t = {k: _dev(torch, inp.get(k), device) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    state = t["h0"].clone()
+    out = torch.empty((T, Bsz, Dm), device=device, dtype=torch.float32)
+
+    def run_all():
+        for s in range(T):
+            ss.selscan_step(t["u"][s], t["delta"][s], t["A"], t["B"][s], t["C"][s], state, D=t["D"], z=t["z"][s],
+                            delta_bias=t["delta_bias"], out=out[s], stream=stream)
+
+    for _ in range(2):
+        state.copy_(t["h0"])
+        run_all()
+    reps = 5
+    times = []
+    for _ in range(reps):
+        state.copy_(t["h0"])
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run_all()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    secs = statistics.median(times)
+    wk = step_work(Bsz, Dm, N)
+    gbs = wk["bytes"] * T / secs / 1e9
+    return {"workload": "decode_step", "batch": Bsz, "dim": Dm, "dstate": N, "steps": T,
+            "elems_per_s": Bsz * Dm * T / secs, "us_per_step": secs / T * 1e6,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
+                         "traffic": recorded_traffic("selscan_step", "decode_step")},
+            "gpu_launches": T * reps}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU arms (the fp64 oracle)
+# ------------------------------------------------------------------------------------------------
+
+def _oracle_rate(inp, rows, nthreads):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.selscan_fwd(inp, rows=rows, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, w, budget_cpu_s=15.0):
+    """The fp64 oracle as it stands on all host cores, on a row sample sized for ~budget_cpu_s of CPU work."""
+    Bsz, Dm, L, N = inp["shape"]
+    cores = os.cpu_count() or 1
+    probe_rows = list(range(min(8, Bsz * Dm)))
+    per_row = _oracle_rate(inp, probe_rows, 1) / len(probe_rows)  # CPU seconds per row on one core
+    nrows = int(max(cores, min(Bsz * Dm, budget_cpu_s / max(per_row, 1e-9))))
+    nrows = min(nrows, Bsz * Dm)
+    rng = np.random.default_rng(7)
+    rows = sorted(rng.choice(Bsz * Dm, size=nrows, replace=False).tolist())
+    secs = _oracle_rate(inp, rows, cores)
+    return {"value": nrows * L / secs, "unit": "elems/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nrows} of {Bsz * Dm} (b,d) rows of {w.name}, each over its full L={L}, N={N}",
+            "seconds": secs}
+
+
+def run_reference(args):
+    """The oracle arm: each step runs the fp64 oracle on a bounded row sample of the workload."""
+    w = si.WORKLOADS[args.workload]
+    inp = si.make_inputs(w)
+    Bsz, Dm, L, N = inp["shape"]
+    cores = os.cpu_count() or 1
+    per_row = _oracle_rate(inp, list(range(min(8, Bsz * Dm))), 1) / min(8, Bsz * Dm)
+    total_steps = args.steps + args.warmup
+    budget_wall = 150.0 / max(total_steps, 1)  # the whole run stays within a few minutes
+    nrows = int(min(Bsz * Dm, max(1, budget_wall * cores / max(per_row, 1e-9))))
+    rng = np.random.default_rng(11)
+    rows = sorted(rng.choice(Bsz * Dm, size=nrows, replace=False).tolist())
+    for _ in range(args.warmup):
+        _oracle_rate(inp, rows, cores)
+    times = [_oracle_rate(inp, rows, cores) for _ in range(args.steps)]
+    secs = sum(times)
+    value = nrows * L * args.steps / secs
+    sample = f"{nrows} of {Bsz * Dm} (b,d) rows of {w.name} per step, each over its full L={L}, N={N}"
+    return {"metric": METRIC, "value": value, "unit": "elems/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "batch": Bsz, "dim": Dm, "seqlen": L, "dstate": N,
+                       "in_dtype": w.in_dtype, "sample_rows_per_step": nrows},
+            "cpu_baseline": {"value": value, "unit": "elems/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "elems/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[n for n in si.WORKLOAD_ORDER
+                                                                     if not si.WORKLOADS[n].steps])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="CPU-seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist_mod
+
+        torch.cuda.set_device(local_rank)
+        dist_mod.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist = dist_mod
+    res = run_ours(args, rank, world, local_rank, dist)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,142 @@
+/*
+ * libselscan — the selective-scan forward of the Mamba selective state-space
+ * model, and its one-token recurrent decode step, on an NVIDIA B300 (sm_103a).
+ *
+ * What is computed, for every batch b, channel d and state index n:
+ *
+ *   Δ_t   = softplus(δ_t + Δ_bias[d])          (or δ_t + Δ_bias[d] when delta_softplus == 0)
+ *   Ā_t   = exp(Δ_t · A[d,n])
+ *   h_t   = Ā_t · h_{t-1} + Δ_t · B[b,n,t] · u_t          (h_{-1} = h0, or 0)
+ *   y_t   = Σ_n C[b,n,t] · h_t[n] + D[d] · u_t
+ *   out_t = y_t · silu(z_t) = y_t · z_t / (1 + e^{-z_t})   (out_t = y_t when z is NULL)
+ *
+ * Sources (web pages on the Mamba selective SSM, cited by title and section):
+ *  - "Mamba状态空间模型深度解析：挑战Transformer的下一代序列建模范式" §2.1 — the
+ *    selective recurrence h_k = A·h_{k-1} + B(x_k)·x_k, y_k = C(x_k)·h_k with B,
+ *    C and Δ functions of the input; §3.1 — the SiLU multiplicative gate.
+ *  - "Mamba架构与SSM模型：高效序列建模技术解析" §2.1 — zero-order hold
+ *    Ā = exp(ΔA); §2.2 — Δ = softplus(Linear(x) + param_Δ).  The Linear
+ *    projection is upstream; its output is the `delta` argument here.
+ *  - "Mamba: Linear-Time Sequence Modeling with Selective SSMs", "连续与离散SSM"
+ *    — y = Cx + Du (the D skip); "选择性扫描要点" — the sequence is scanned in
+ *    blocks whose end state is passed on as the next block's start state,
+ *    which is exactly what h0 / h_last expose across calls.
+ *  - "Mamba架构深度剖析：如何以线性时间重塑序列建模" §3 — recurrent (RNN-mode)
+ *    inference with a constant-size state: selscan_step.
+ * The input matrix is discretised as B̄ = Δ·B (not the exact zero-order-hold
+ * form (ΔA)^{-1}(exp(ΔA) - I)·ΔB that the same §2.1 also prints).
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are DEVICE pointers (cudaMalloc'd, or pinned host
+ *    memory mapped into the device address space) to contiguous row-major
+ *    arrays, last index fastest.  The caller owns every buffer; the library
+ *    allocates no device memory and keeps no state between calls.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  A return of SELSCAN_OK means the work was
+ *    enqueued; faults during execution surface at the caller's next
+ *    synchronisation, as for any CUDA launch.
+ *  - Arguments are checked on the host before anything is enqueued.  A bad
+ *    argument returns an error status and enqueues nothing.  Each pointer must
+ *    be device-accessible and lie, with its whole extent, inside one device
+ *    allocation (checked with the driver's address-range query).
+ *  - Element types: u, delta, z, B, C are `in_dtype` (fp32 or bf16); out is
+ *    `out_dtype`; A, D, delta_bias, h0, h_last and the decode state are fp32.
+ *  - Optional arguments may be NULL: D (treated as 0), z (no gate),
+ *    delta_bias (0), h0 (zero start state), h_last (not written).
+ *  - h_last may alias h0 (in-place carry).  No other output may overlap an
+ *    input (SELSCAN_ERR_ALIAS).
+ *  - Thread safety: calls from several host threads are safe; calls on the
+ *    same stream run in order.
+ */
+#ifndef SELSCAN_H_
+#define SELSCAN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SELSCAN_ABI_VERSION 1
+#define SELSCAN_MAX_DSTATE 16
+
+typedef enum { SELSCAN_F32 = 0, SELSCAN_BF16 = 1 } selscan_dtype_t;
+
+typedef enum {
+  SELSCAN_OK = 0,
+  SELSCAN_ERR_NULL = 1,        /* a required pointer (or the shape) is NULL */
+  SELSCAN_ERR_SHAPE = 2,       /* negative size, dstate < 1, or a size product overflows */
+  SELSCAN_ERR_ALIGN = 3,       /* a pointer is not aligned to its element size */
+  SELSCAN_ERR_UNSUPPORTED = 4, /* dstate > SELSCAN_MAX_DSTATE or an unknown dtype */
+  SELSCAN_ERR_CUDA = 5,        /* a CUDA call failed; see selscan_last_cuda_error() */
+  SELSCAN_ERR_POINTER = 6,     /* a pointer is not device-accessible or its extent leaves its allocation */
+  SELSCAN_ERR_ALIAS = 7        /* an output overlaps an input (other than h_last == h0) */
+} selscan_status_t;
+
+/* Problem sizes.  For selscan_step, seqlen must be 1. */
+typedef struct {
+  int64_t batch;  /* B */
+  int64_t dim;    /* D, the channel (d_inner) count */
+  int64_t seqlen; /* L */
+  int64_t dstate; /* N, 1 .. SELSCAN_MAX_DSTATE */
+  selscan_dtype_t in_dtype;  /* type of u, delta, z, B, C */
+  selscan_dtype_t out_dtype; /* type of out */
+} selscan_shape_t;
+
+/*
+ * Selective-scan forward over a whole sequence.
+ *
+ *   u, delta, z : [B, D, L]  in_dtype     input, pre-softplus Δ, gate (z nullable)
+ *   A           : [D, N]     fp32         diagonal state matrix (usually negative)
+ *   B, C        : [B, N, L]  in_dtype     input-dependent input / output matrices,
+ *                                         shared by all D channels of a batch row
+ *   D           : [D]        fp32         skip weight (nullable)
+ *   delta_bias  : [D]        fp32         added to delta before the softplus (nullable)
+ *   delta_softplus : nonzero applies softplus to δ + Δ_bias
+ *   h0          : [B, D, N]  fp32         start state (nullable: zeros)
+ *   out         : [B, D, L]  out_dtype    gated output
+ *   h_last      : [B, D, N]  fp32         state after the last step (nullable; may alias h0)
+ *
+ * Splitting a sequence into consecutive calls, each given the previous call's
+ * h_last as h0, gives the same result as one call up to fp32 rounding.
+ * L = 0 writes h_last = h0 (or zeros) and nothing else.
+ */
+selscan_status_t selscan_fwd(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* delta_bias, int delta_softplus, const float* h0, void* out,
+                             float* h_last, void* stream);
+
+/*
+ * One recurrent decode step (the L = 1 case of the forward, done in place on
+ * the state).  Shapes: u, delta, z, out [B, D]; B, C [B, N]; A [D, N];
+ * D, delta_bias [D]; state [B, D, N] fp32, read as h_{t-1} and overwritten
+ * with h_t.  shape->seqlen must be 1.  `state` must not overlap any input.
+ */
+selscan_status_t selscan_step(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                              const void* B, const void* C, const float* D, const void* z,
+                              const float* delta_bias, int delta_softplus, float* state, void* out,
+                              void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* selscan_status_string(selscan_status_t status);
+
+/* The cudaError_t of the last SELSCAN_ERR_CUDA returned on this host thread (0 if none). */
+int selscan_last_cuda_error(void);
+
+/*
+ * Device-side status of earlier launches on the current device: 0 if every launch ran to completion,
+ * 1 if a kernel gave up a bounded wait for one of its own asynchronous shared-memory copies (it then
+ * stops early and leaves its outputs incomplete, instead of waiting forever).  `reset` != 0 clears
+ * the word.  The read is a synchronous device-to-host copy: it waits for work already enqueued on
+ * the legacy default stream.  Returns -1 if the read itself fails.
+ */
+int selscan_device_status(int reset);
+
+/* SELSCAN_ABI_VERSION of the library that is loaded. */
+int selscan_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SELSCAN_H_ */

@@ -1,0 +1,199 @@
+"""Python binding of libselscan (selective-scan forward and recurrent decode step on B300).
+
+The functions here only marshal arguments: they check tensor types and
+layouts, allocate missing outputs with torch, and call the C ABI declared in
+``include/selscan.h``.  Every step of the computation runs in the library's
+CUDA kernels.  There is no CPU or PyTorch fallback: if ``libselscan.so`` has
+not been built, every call raises.
+
+Build the library with ``python -m selective_state_space_152_b300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libselscan.so")
+
+SELSCAN_F32, SELSCAN_BF16 = 0, 1
+STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SELSCAN_ERR_ALIGN",
+          4: "SELSCAN_ERR_UNSUPPORTED", 5: "SELSCAN_ERR_CUDA", 6: "SELSCAN_ERR_POINTER", 7: "SELSCAN_ERR_ALIAS"}
+EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
+            "selscan_abi_version")
+
+
+class SelscanError(RuntimeError):
+    """A libselscan entry point returned a status other than SELSCAN_OK."""
+
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class SelscanShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load libselscan.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libselscan.so not found at {p}; build it with "
+                           "`python -m selective_state_space_152_b300.build`")
+    lib = ctypes.CDLL(p)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    shp = ctypes.POINTER(SelscanShape)
+    lib.selscan_fwd.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
+    lib.selscan_fwd.restype = i32
+    lib.selscan_step.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
+    lib.selscan_step.restype = i32
+    lib.selscan_status_string.argtypes = [i32]
+    lib.selscan_status_string.restype = ctypes.c_char_p
+    lib.selscan_last_cuda_error.argtypes = []
+    lib.selscan_last_cuda_error.restype = i32
+    lib.selscan_device_status.argtypes = [i32]
+    lib.selscan_device_status.restype = i32
+    lib.selscan_abi_version.argtypes = []
+    lib.selscan_abi_version.restype = i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def selscan_status_string(status: int) -> str:
+    return load_library().selscan_status_string(int(status)).decode()
+
+
+def selscan_abi_version() -> int:
+    return load_library().selscan_abi_version()
+
+
+def selscan_last_cuda_error() -> int:
+    return load_library().selscan_last_cuda_error()
+
+
+def selscan_device_status(reset: bool = False) -> int:
+    """0 if no kernel gave up a bounded wait since the last reset (synchronous read)."""
+    return load_library().selscan_device_status(int(bool(reset)))
+
+
+def _check(status: int):
+    if status != 0:
+        msg = selscan_status_string(status)
+        if status == 5:
+            msg += f" (cudaError {selscan_last_cuda_error()})"
+        raise SelscanError(status, msg)
+
+
+def _torch():
+    import torch  # torch supplies device memory and streams only
+
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t == torch.float32:
+        return SELSCAN_F32
+    if t == torch.bfloat16:
+        return SELSCAN_BF16
+    raise TypeError(f"unsupported dtype {t}; use torch.float32 or torch.bfloat16")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libselscan takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libselscan takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _need_f32(name, t):
+    torch = _torch()
+    if t is not None and t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+
+
+def selscan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
+                out=None, h_last=None, stream=None, out_dtype=None, return_h_last: bool = False):
+    """Selective-scan forward (see ``include/selscan.h``).
+
+    u, delta, z: [B, D, L]; B, C: [B, N, L] (all float32 or all bfloat16);
+    A: [D, N], D / delta_bias: [D], h0 / h_last: [B, D, N] (float32).
+    ``out`` ([B, D, L]) is allocated if not given, with ``out_dtype``
+    (default float32).  ``h_last`` is allocated when ``return_h_last``.
+    Returns ``(out, h_last)`` (``h_last`` may be None).  The work is enqueued
+    on ``stream`` (default: torch's current stream).
+    """
+    torch = _torch()
+    lib = load_library()
+    if u.dim() != 3 or B.dim() != 3:
+        raise ValueError("u must be [B, D, L] and B must be [B, N, L]")
+    Bsz, Dm, L = u.shape
+    N = B.shape[1]
+    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias), ("h0", h0), ("h_last", h_last)):
+        _need_f32(name, t)
+    for name, t in (("delta", delta), ("z", z), ("B", B), ("C", C)):
+        if t is not None and t.dtype != u.dtype:
+            raise TypeError(f"{name} must have u's dtype {u.dtype}")
+    if out is None:
+        out = torch.empty((Bsz, Dm, L), device=u.device, dtype=out_dtype or torch.float32)
+    if h_last is None and return_h_last:
+        h_last = torch.empty((Bsz, Dm, N), device=u.device, dtype=torch.float32)
+    shape = SelscanShape(Bsz, Dm, L, N, _dtype_code(u.dtype), _dtype_code(out.dtype))
+    st = lib.selscan_fwd(ctypes.byref(shape), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                         _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(out), _ptr(h_last),
+                         _stream_handle(stream))
+    _check(st)
+    return out, h_last
+
+
+def selscan_step(u, delta, A, B, C, state, D=None, z=None, delta_bias=None, delta_softplus: bool = True,
+                 out=None, stream=None, out_dtype=None):
+    """One recurrent decode step, updating ``state`` [B, D, N] (float32) in place.
+
+    u, delta, z: [B, D]; B, C: [B, N]; returns ``out`` [B, D].
+    """
+    torch = _torch()
+    lib = load_library()
+    if u.dim() != 2 or B.dim() != 2:
+        raise ValueError("u must be [B, D] and B must be [B, N]")
+    Bsz, Dm = u.shape
+    N = B.shape[1]
+    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias), ("state", state)):
+        _need_f32(name, t)
+    for name, t in (("delta", delta), ("z", z), ("B", B), ("C", C)):
+        if t is not None and t.dtype != u.dtype:
+            raise TypeError(f"{name} must have u's dtype {u.dtype}")
+    if out is None:
+        out = torch.empty((Bsz, Dm), device=u.device, dtype=out_dtype or torch.float32)
+    shape = SelscanShape(Bsz, Dm, 1, N, _dtype_code(u.dtype), _dtype_code(out.dtype))
+    st = lib.selscan_step(ctypes.byref(shape), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                          _ptr(delta_bias), int(bool(delta_softplus)), _ptr(state), _ptr(out),
+                          _stream_handle(stream))
+    _check(st)
+    return out
+
+
+__all__ = ["selscan_fwd", "selscan_step", "selscan_status_string", "selscan_abi_version",
+           "selscan_last_cuda_error", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED"]

@@ -1,0 +1,454 @@
+// Selective-scan forward for problems with many (batch, channel) rows: sequential in t, no scan.
+//
+// Same computation as the chunked kernel in selscan_fwd.cu (see include/selscan.h): per row (b, d)
+// and state n, Δ_t = softplus(δ_t + Δ_bias[d]), h_t = exp(Δ_t A[d,n]) h_{t-1} + Δ_t B[b,n,t] u_t,
+// y_t = Σ_n C[b,n,t] h_t + D[d] u_t, out_t = y_t silu(z_t)  ("Mamba状态空间模型深度解析" §2.1, §3.1;
+// "Mamba架构与SSM模型：高效序列建模技术解析" §2.1, §2.2).  This is the recurrent form run directly:
+// every lane walks its row from t = 0 to L-1, so no step is computed twice and no lanes have to be
+// joined by a scan.  The parallelism comes from the rows: Q lanes share a row, each owning
+// SPL = NS/Q of its states (Q = 2 for 16 states), and a warp holds 32/Q rows.
+//
+// Per step and lane, the states are taken in pairs (n, n+1) as float2:
+//   Ā = 2^(Δ·(A_n, A_n+1)·log2 e),  h = Ā ⊙ h + Δu·(B_n, B_n+1),  y2 += (C_n, C_n+1) ⊙ h
+// so the only dependency from one step to the next is one packed FMA per state pair; the
+// exponentials of later steps are independent of the state and overlap with it.  The Q partial sums
+// of y meet with a shuffle.
+//
+// Every input of a chunk of T steps is fetched by the tensor memory accelerator one chunk ahead (1-D
+// bulk copies, one per row): the CTA's rows of u, δ and z, and the raw [n][t] rows of B and C.  B and C
+// are then transposed once per CTA into a [t][n] fp32 tile, so that the B (or C) values of one step
+// and one lane's states are one 128-bit shared load that every lane of a quarter-warp reads at the
+// same address (a broadcast).  The u, δ, z rows are stored with a 16-byte pad per row so that the
+// rows read by one quarter-warp fall in different bank groups.
+#include <cstring>
+
+#include "selscan_internal.cuh"
+
+namespace selscan {
+
+// Set by a kernel whose bounded wait on a bulk copy gave up (read by selscan_device_status()).
+__device__ int g_selscan_seq_error = 0;
+
+namespace {
+
+template <int NS, int Q, int R, typename Tin>
+struct SeqCfg {
+  static constexpr int SPL = NS / Q;  // states per lane
+  static constexpr int PAIRS = SPL / 2;
+  static constexpr int RPW = 32 / Q;    // rows per warp
+  static constexpr int ROWS = R * RPW;  // rows per CTA
+  static constexpr int T = 64;          // steps per chunk
+  static constexpr int SB = 8;          // steps per sub-block
+  static constexpr int TS = NS + 4;     // floats per step in the tile (padded: transposing stores spread over banks)
+  static constexpr int EPR = 128 / static_cast<int>(sizeof(Tin));  // inputs per 128-byte swizzled stage row
+  static constexpr int SUBT = T / EPR;                            // stage sub-tiles per tensor and chunk
+  static constexpr int UDZ = 3 * T * ROWS;  // elements of one u, δ, z stage: [3][SUBT][ROWS][EPR]
+  static constexpr int RAW = 2 * NS * T;    // raw elements of one chunk: B rows then C rows, [2][NS][T]
+  static constexpr int TILE = 2 * T * TS;   // floats of one transposed tile: [2][T][TS]
+  static constexpr size_t kUdzBytes = 2 * UDZ * sizeof(Tin);       // double-buffered
+  static constexpr size_t kRawBytes = 2 * RAW * sizeof(Tin);       // double-buffered
+  static constexpr size_t kTileBytes = 2 * TILE * sizeof(float);  // double-buffered
+  // + 1 KiB so that the stage can start on a 1 KiB boundary (the 128-byte swizzle pattern repeats
+  // every 8 rows of 128 bytes and is computed from the address).
+  static constexpr size_t kSmem = 1024 + kUdzBytes + kRawBytes + kTileBytes + 2 * sizeof(uint64_t);
+  static_assert(SPL >= 4 && SPL % 4 == 0, "each lane owns whole groups of 4 states");
+  static_assert((ROWS * 128) % 1024 == 0, "stage sub-tiles must keep 1 KiB alignment");
+};
+
+// 8 consecutive inputs of a row as 16-byte vectors.
+template <typename T>
+struct Vec8 {
+  static constexpr int kPerVec = 16 / sizeof(T);
+  static constexpr int kVecs = 8 / kPerVec;
+  uint4 v[kVecs];
+  __device__ __forceinline__ float get(int i) const { return elem_of(v[i / kPerVec], i % kPerVec, T()); }
+};
+
+template <typename T>
+__device__ __forceinline__ void load8(Vec8<T>& s, const T* __restrict__ row, int64_t t, int64_t L, bool vec) {
+  constexpr int kPerVec = Vec8<T>::kPerVec;
+  if (vec && t + 8 <= L) {
+#pragma unroll
+    for (int q = 0; q < Vec8<T>::kVecs; q++) s.v[q] = __ldg(reinterpret_cast<const uint4*>(row + t) + q);
+  } else {
+#pragma unroll
+    for (int q = 0; q < Vec8<T>::kVecs; q++) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int k = 0; k < kPerVec; k++) {
+        const int64_t tt = t + q * kPerVec + k;
+        const uint32_t bits = tt < L ? raw_bits(row, tt) : 0u;
+        if (sizeof(T) == 4) w[k] = bits;
+        else w[k >> 1] |= (k & 1) ? (bits << 16) : bits;
+      }
+      s.v[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store8(T* __restrict__ row, int64_t t, int64_t L, bool vec, const float (&y)[8]) {
+  constexpr int kPerVec = 16 / sizeof(T);
+  if (vec && t + 8 <= L) {
+#pragma unroll
+    for (int q = 0; q < 8 / kPerVec; q++) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int k = 0; k < kPerVec; k++) {
+        const uint32_t bits = out_bits(y[q * kPerVec + k], T());
+        if (sizeof(T) == 4) w[k] = bits;
+        else w[k >> 1] |= (k & 1) ? (bits << 16) : bits;
+      }
+      reinterpret_cast<uint4*>(row + t)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+      if (t + i < L) row[t + i] = from_f32<T>(y[i]);
+  }
+}
+
+// 8 consecutive staged inputs [t, t+8) of CTA row r from a tensor's stage [SUBT][ROWS][EPR], written
+// by a 2-D tensor copy with the 128-byte swizzle: 16-byte chunk c of stage row r sits at chunk
+// position c ^ (r mod 8).  Steps past the end of the sequence were zero-filled by the copy.
+template <typename T, int ROWS>
+__device__ __forceinline__ void stage8(Vec8<T>& s, const unsigned char* __restrict__ stage, int r, int t) {
+  constexpr int kPerVec = Vec8<T>::kPerVec, EPR = 128 / static_cast<int>(sizeof(T));
+#pragma unroll
+  for (int q = 0; q < Vec8<T>::kVecs; q++) {
+    const int e = t + q * kPerVec;
+    const int sub = e / EPR, chunk = (e % EPR) / kPerVec;
+    s.v[q] = *reinterpret_cast<const uint4*>(stage + (sub * ROWS + r) * 128 + ((chunk ^ (r & 7)) << 4));
+  }
+}
+
+// Transpose raw chunk rows [2][NS][T] (Tin) into the tile [2][T][TS] (fp32), zeroing states >= N and
+// steps >= L.  Work unit: one tensor, 4 states, 4 steps (steps fastest across threads).
+template <int NS, int Q, int R, typename Tin, bool MASK>
+__device__ __forceinline__ void transpose_chunk(const Tin* __restrict__ rb, float* __restrict__ tb, int tid,
+                                                int64_t t0, int64_t L, int N) {
+  using C = SeqCfg<NS, Q, R, Tin>;
+  constexpr int T4 = C::T / 4, N4 = NS / 4, UNITS = 2 * N4 * T4;
+  for (int unit = tid; unit < UNITS; unit += R * 32) {
+    const int t4 = unit % T4, rest = unit / T4;
+    const int n4 = rest % N4, tt = rest / N4;
+    float v[4][4];  // [state k][step m]
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const Tin* src = rb + (tt * NS + n4 * 4 + k) * C::T + t4 * 4;
+      if (sizeof(Tin) == 2) {
+        const uint2 w = *reinterpret_cast<const uint2*>(src);
+        v[k][0] = __uint_as_float(w.x << 16);
+        v[k][1] = __uint_as_float(w.x & 0xffff0000u);
+        v[k][2] = __uint_as_float(w.y << 16);
+        v[k][3] = __uint_as_float(w.y & 0xffff0000u);
+      } else {
+        const float4 w = *reinterpret_cast<const float4*>(src);
+        v[k][0] = w.x;
+        v[k][1] = w.y;
+        v[k][2] = w.z;
+        v[k][3] = w.w;
+      }
+      if (MASK) {
+#pragma unroll
+        for (int m = 0; m < 4; m++)
+          if (n4 * 4 + k >= N || t0 + t4 * 4 + m >= L) v[k][m] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+      *reinterpret_cast<float4*>(tb + tt * C::T * C::TS + (t4 * 4 + m) * C::TS + n4 * 4) =
+          make_float4(v[0][m], v[1][m], v[2][m], v[3][m]);
+  }
+}
+
+#ifndef SELSCAN_SEQ_WARPS_PER_SM
+#define SELSCAN_SEQ_WARPS_PER_SM 12
+#endif
+
+template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
+__global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
+    selscan_fwd_seq_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
+  using C = SeqCfg<NS, Q, R, Tin>;
+  constexpr int T = C::T, SB = C::SB, TS = C::TS, SPL = C::SPL, PAIRS = C::PAIRS, RPW = C::RPW;
+  extern __shared__ __align__(128) unsigned char smem_dyn[];
+  unsigned char* smem_base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* udz = smem_base;                                           // [2 buffers][3][SUBT][ROWS][EPR]
+  Tin* raw = reinterpret_cast<Tin*>(smem_base + C::kUdzBytes);              // [2 buffers][2][NS][T]
+  float* tiles = reinterpret_cast<float*>(smem_base + C::kUdzBytes + C::kRawBytes);  // [2 buffers][2][T][TS]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_base + C::kUdzBytes + C::kRawBytes + C::kTileBytes);
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int q = lane / RPW;  // state group: states [q·SPL, (q+1)·SPL)
+  const int rw = lane % RPW;
+  const int64_t b = blockIdx.y;
+  const int64_t d = static_cast<int64_t>(blockIdx.x) * C::ROWS + (tid >> 5) * RPW + rw;
+  const bool row_ok = d < p.dim;
+  const int N = FULLN ? NS : p.dstate;
+  const int64_t L = p.seqlen;
+  const int64_t nchunks = (L + T - 1) / T;
+  const Tin* __restrict__ Bsrc = static_cast<const Tin*>(p.B) + b * N * L;
+  const Tin* __restrict__ Csrc = static_cast<const Tin*>(p.C) + b * N * L;
+  const bool tma = p.use_tma;
+
+  // Issue the five 2-D tensor copies of chunk c into buffer c & 1 (one thread): the B and C rows of
+  // batch entry b, and the CTA's rows of u, δ, z.  Parts of a box past the end of a tensor are
+  // zero-filled and still count towards the expected bytes.
+  const int row0 = static_cast<int>(b * p.dim + static_cast<int64_t>(blockIdx.x) * C::ROWS);
+  const int ntens = p.z ? 3 : 2;
+  auto issue = [&](int64_t c) {
+    const int t0 = static_cast<int>(c * T);
+    uint64_t* bar = &bars[c & 1];
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(bar, static_cast<uint32_t>((2 * NS + ntens * C::ROWS) * T * sizeof(Tin)));
+    Tin* dst = raw + (c & 1) * C::RAW;
+    tma_load_2d(dst, &maps.B, t0, static_cast<int>(b * N), bar);
+    tma_load_2d(dst + NS * T, &maps.C, t0, static_cast<int>(b * N), bar);
+    unsigned char* st = udz + (c & 1) * (C::UDZ * sizeof(Tin));
+    const CUtensorMap* m[3] = {&maps.u, &maps.delta, &maps.z};
+    for (int k = 0; k < ntens; k++)
+      for (int sub = 0; sub < C::SUBT; sub++)
+        tma_load_2d(st + (k * C::SUBT + sub) * C::ROWS * 128, m[k], t0 + sub * C::EPR, row0, bar);
+  };
+
+  if (tid == 0) {
+    s_abort = 0;
+    if (tma) {
+      mbar_init(&bars[0], 1);
+      mbar_init(&bars[1], 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+  }
+  __syncthreads();
+  if (tma && tid == 0 && nchunks > 0) issue(0);
+
+  // This lane's states, in pairs: state n0 + 2i and n0 + 2i + 1.
+  const int n0 = q * SPL;
+  float2 A2[PAIRS], h[PAIRS];
+#pragma unroll
+  for (int i = 0; i < PAIRS; i++) {
+    float a[2], hh[2];
+#pragma unroll
+    for (int k = 0; k < 2; k++) {
+      const int n = n0 + 2 * i + k;
+      const bool ok = row_ok && n < N;
+      a[k] = ok ? p.A[d * N + n] * kLog2e : 0.f;
+      hh[k] = (ok && p.h0) ? p.h0[(b * p.dim + d) * N + n] : 0.f;
+    }
+    A2[i] = f2(a[0], a[1]);
+    h[i] = f2(hh[0], hh[1]);
+  }
+  const float bias = (row_ok && p.delta_bias) ? p.delta_bias[d] : 0.f;
+  const float Dd = (row_ok && p.D) ? p.D[d] : 0.f;
+  // Rows past `dim` (tail of the last CTA) run on row 0's inputs so that every lane takes part in
+  // the shuffles; only their stores are skipped.
+  const int64_t row_off = (b * p.dim + (row_ok ? d : 0)) * L;
+  const Tin* __restrict__ u_row = static_cast<const Tin*>(p.u) + row_off;
+  const Tin* __restrict__ dl_row = static_cast<const Tin*>(p.delta) + row_off;
+  const Tin* __restrict__ z_row = p.z ? static_cast<const Tin*>(p.z) + row_off : nullptr;
+  Tout* __restrict__ o_row = static_cast<Tout*>(p.out) + row_off;
+  const bool vec = p.vec_in && p.vec_out;
+
+  int64_t c = 0;
+  for (; c < nchunks; c++) {
+    const int64_t t0 = c * T;
+    const Tin* rb = raw + (c & 1) * C::RAW;
+    float* tb = tiles + (c & 1) * C::TILE;
+    const bool tail = t0 + T > L;
+    if (tma) {
+      if (!mbar_wait(&bars[c & 1], static_cast<uint32_t>((c >> 1) & 1))) s_abort = 1;
+    } else {
+      Tin* wb = raw + (c & 1) * C::RAW;
+      for (int e = tid; e < C::RAW; e += R * 32) {
+        const int rowi = e / T, tt = e - rowi * T;
+        const int n = rowi < NS ? rowi : rowi - NS;
+        const Tin* srcp = rowi < NS ? Bsrc : Csrc;
+        wb[e] = (n < N && t0 + tt < L) ? srcp[n * L + t0 + tt] : from_f32<Tin>(0.f);
+      }
+      __syncthreads();
+    }
+    if (FULLN && !tail)
+      transpose_chunk<NS, Q, R, Tin, false>(rb, tb, tid, t0, L, N);
+    else
+      transpose_chunk<NS, Q, R, Tin, true>(rb, tb, tid, t0, L, N);
+    __syncthreads();  // tile c complete; every warp has finished chunk c-1
+    if (s_abort) break;
+    if (tma && tid == 0 && c + 1 < nchunks) issue(c + 1);
+
+    const float* tB = tb + n0;
+    const float* tC = tb + T * TS + n0;
+    // This lane's row of the staged u, δ, z (rows past `dim` hold zeros or the next batch entry's
+    // rows: computed on, never stored).
+    const int r_cta = (tid >> 5) * RPW + rw;
+    const unsigned char* su = udz + (c & 1) * (C::UDZ * sizeof(Tin));
+    const unsigned char* sd = su + C::SUBT * C::ROWS * 128;
+    const unsigned char* sz = sd + C::SUBT * C::ROWS * 128;
+#pragma unroll 1
+    for (int sb = 0; sb < T; sb += SB) {
+      const int64_t ts = t0 + sb;
+      if (ts >= L) break;
+      const bool full = !tail || ts + SB <= L;
+      float dl[SB], du[SB], y[SB];
+      {
+        Vec8<Tin> us, ds;
+        if (tma) {
+          stage8<Tin, C::ROWS>(us, su, r_cta, sb);
+          stage8<Tin, C::ROWS>(ds, sd, r_cta, sb);
+        } else {
+          load8<Tin>(us, u_row, ts, L, vec && full);
+          load8<Tin>(ds, dl_row, ts, L, vec && full);
+        }
+        // Straight-line over the 8 steps (no branches), so their exponential/log chains overlap.
+#pragma unroll
+        for (int i = 0; i < SB; i++) {
+          const float x = ds.get(i) + bias;
+          float delta = SOFTPLUS ? softplus_fast(x) : x;
+          delta = (full || ts + i < L) ? delta : 0.f;  // identity steps past the end
+          const float uu = us.get(i);
+          dl[i] = delta;
+          du[i] = delta * uu;
+          y[i] = Dd * uu;
+        }
+      }
+      float part[SB];
+#pragma unroll
+      for (int i = 0; i < SB; i++) {
+        const float2 dd = f2(dl[i], dl[i]), uu = f2(du[i], du[i]);
+        const float4* bq = reinterpret_cast<const float4*>(tB + (sb + i) * TS);
+        const float4* cq = reinterpret_cast<const float4*>(tC + (sb + i) * TS);
+        float2 yp = f2(0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < SPL / 4; g++) {
+          const float4 bb = bq[g], cc = cq[g];
+#pragma unroll
+          for (int k = 0; k < 2; k++) {
+            const int pi = 2 * g + k;
+            const float2 e = mul2s(dd, A2[pi]);
+            const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
+            h[pi] = fma2s(ab, h[pi], mul2s(uu, k ? f2(bb.z, bb.w) : f2(bb.x, bb.y)));
+            yp = fma2s(k ? f2(cc.z, cc.w) : f2(cc.x, cc.y), h[pi], yp);
+          }
+        }
+        part[i] = yp.x + yp.y;
+      }
+      // The row's Q lanes each hold the sum over their states: add them up (8 independent shuffles).
+#pragma unroll
+      for (int o = RPW; o < 32; o <<= 1)
+#pragma unroll
+        for (int i = 0; i < SB; i++) part[i] += __shfl_xor_sync(kFull, part[i], o);
+#pragma unroll
+      for (int i = 0; i < SB; i++) y[i] += part[i];
+      if (z_row) {
+        Vec8<Tin> zs;
+        if (tma) stage8<Tin, C::ROWS>(zs, sz, r_cta, sb);
+        else load8<Tin>(zs, z_row, ts, L, vec && full);
+#pragma unroll
+        for (int i = 0; i < SB; i++) y[i] *= silu_fast(zs.get(i));
+      }
+      if (row_ok && q == 0) store8<Tout>(o_row, ts, L, vec && full, y);
+    }
+  }
+
+  if (s_abort) {
+    if (tid == 0) {
+      atomicExch(&g_selscan_seq_error, 1);
+      mbar_wait(&bars[c & 1], static_cast<uint32_t>((c >> 1) & 1));
+    }
+    return;
+  }
+  if (row_ok && p.h_last) {
+#pragma unroll
+    for (int i = 0; i < PAIRS; i++)
+#pragma unroll
+      for (int k = 0; k < 2; k++) {
+        const int n = n0 + 2 * i + k;
+        if (n < N) p.h_last[(b * p.dim + d) * N + n] = k ? h[i].y : h[i].x;
+      }
+  }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// A 2-D map of a row-major [rows][inner] tensor with box [box_rows][box_inner] (inner fastest).
+template <typename Tin>
+bool encode_2d(EncodeTiled enc, CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+               uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * sizeof(Tin)};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
+cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
+  using C = SeqCfg<NS, Q, R, Tin>;
+  FwdParams p = p_in;
+  TmaMaps maps;
+  memset(&maps, 0, sizeof maps);
+  // Tensor copies need 16-byte aligned rows (vec_stage) and coordinates that fit in 32 bits.
+  const EncodeTiled enc = reinterpret_cast<EncodeTiled>(tensor_map_encoder());
+  const uint64_t rows = static_cast<uint64_t>(p.batch * p.dim), bc_rows = static_cast<uint64_t>(p.batch * p.dstate);
+  p.use_tma = p.vec_stage && enc && rows < (1ull << 31) && p.seqlen < (1ll << 31);
+  if (p.use_tma) {
+    const uint64_t L = static_cast<uint64_t>(p.seqlen);
+    bool ok = encode_2d<Tin>(enc, &maps.u, p.u, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d<Tin>(enc, &maps.delta, p.delta, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              (!p.z || encode_2d<Tin>(enc, &maps.z, p.z, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+              encode_2d<Tin>(enc, &maps.B, p.B, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              encode_2d<Tin>(enc, &maps.C, p.C, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE);
+    p.use_tma = ok;
+  }
+  auto kern = selscan_fwd_seq_kernel<NS, Q, R, Tin, Tout, FULLN, SOFTPLUS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>((p.dim + C::ROWS - 1) / C::ROWS), static_cast<unsigned>(p.batch));
+  kern<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+  return cudaGetLastError();
+}
+
+#ifndef SELSCAN_SEQ_R
+#define SELSCAN_SEQ_R 2
+#endif
+
+template <typename Tin, typename Tout, bool SOFTPLUS>
+cudaError_t dispatch_seq_sp(const FwdParams& p, cudaStream_t s) {
+  constexpr int R = SELSCAN_SEQ_R;
+  if (p.dstate == 16) return launch_seq_cfg<16, 2, R, Tin, Tout, true, SOFTPLUS>(p, s);
+  if (p.dstate <= 4) return launch_seq_cfg<4, 1, R, Tin, Tout, false, SOFTPLUS>(p, s);
+  if (p.dstate <= 8) return launch_seq_cfg<8, 2, R, Tin, Tout, false, SOFTPLUS>(p, s);
+  return launch_seq_cfg<16, 2, R, Tin, Tout, false, SOFTPLUS>(p, s);
+}
+
+template <typename Tin, typename Tout>
+cudaError_t dispatch_seq(const FwdParams& p, cudaStream_t s) {
+  return p.delta_softplus ? dispatch_seq_sp<Tin, Tout, true>(p, s) : dispatch_seq_sp<Tin, Tout, false>(p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s) {
+  if (in_dtype == SELSCAN_F32) {
+    return out_dtype == SELSCAN_F32 ? dispatch_seq<float, float>(p, s) : dispatch_seq<float, __nv_bfloat16>(p, s);
+  }
+  return out_dtype == SELSCAN_F32 ? dispatch_seq<__nv_bfloat16, float>(p, s)
+                                  : dispatch_seq<__nv_bfloat16, __nv_bfloat16>(p, s);
+}
+
+cudaError_t read_seq_device_error(int* value, int reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_selscan_seq_error, sizeof(int));
+  if (e == cudaSuccess && reset) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_selscan_seq_error, &zero, sizeof(int));
+  }
+  return e;
+}
+
+}  // namespace selscan

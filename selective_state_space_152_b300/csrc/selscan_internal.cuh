@@ -1,0 +1,270 @@
+// Internal declarations shared by the libselscan CUDA sources (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (declarations only: the library does not link libcuda)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "selscan.h"
+
+namespace selscan {
+
+// Arguments of one selscan_fwd launch, already validated on the host.
+struct FwdParams {
+  int64_t batch, dim, seqlen;
+  int dstate;
+  const void* u;
+  const void* delta;
+  const void* z;  // nullable
+  const void* B;
+  const void* C;
+  const float* A;
+  const float* D;           // nullable
+  const float* delta_bias;  // nullable
+  const float* h0;          // nullable
+  void* out;
+  float* h_last;  // nullable
+  int delta_softplus;
+  int vec_in;   // u, delta, z rows may be read with 16-byte vectors
+  int vec_out;  // out rows may be written with 16-byte vectors
+  int vec_bc;   // B, C rows may be read with 16-byte vectors (and bulk-copied)
+  int vec_stage;  // B, C and u, delta, z rows may all be bulk-copied
+  int use_tma;    // set by a launcher: its kernel stages inputs with tensor copies
+};
+
+// Arguments of one selscan_step launch.
+struct StepParams {
+  int64_t batch, dim;
+  int dstate;
+  const void* u;
+  const void* delta;
+  const void* z;
+  const void* B;
+  const void* C;
+  const float* A;
+  const float* D;
+  const float* delta_bias;
+  float* state;
+  void* out;
+  int delta_softplus;
+  int vec_state;  // state / A rows may be accessed as float4 (dstate % 4 == 0, 16-byte aligned)
+};
+
+cudaError_t launch_fwd(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
+
+// Tensor maps (2-D TMA descriptors) of one forward call: u, delta, z by rows of the CTA, B and C by the
+// dstate rows of a batch entry.  Passed to the kernel as a __grid_constant__ parameter.
+struct alignas(64) TmaMaps {
+  CUtensorMap u, delta, z, B, C;
+};
+// cuTensorMapEncodeTiled, fetched through the runtime (nullptr if the driver does not provide it).
+void* tensor_map_encoder();
+cudaError_t launch_step(const StepParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
+// The sequential forward kernel (rows-parallel, no scan) used by launch_fwd for many-row problems.
+cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
+// Read (and optionally clear) the device-side failure words set by a kernel's bounded wait.
+cudaError_t read_device_error(int* value, int reset);
+cudaError_t read_seq_device_error(int* value, int reset);
+
+// ---------------------------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------------------------
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x on the special-function unit (approximate, flushes subnormal results to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// softplus(x) = log(1 + e^x).  Above 20 the result equals x to within 2.1e-9 absolute.
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(__expf(x)); }
+
+// silu(z) = z / (1 + e^{-z}); for z below about -88 the quotient underflows to -0.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+
+// ---- helpers shared by the forward kernels -------------------------------------------------------
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr long long kWaitLimit = 1ll << 26;  // polls of an mbarrier before a copy is declared lost
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float r;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// softplus(x) = max(x, 0) + log1p(e), e = exp(-|x|) ∈ (0, 1].
+// For e ≥ 1/16, log1p(e) = log2(1 + e)·ln 2 on the special-function unit: 1 + e ≥ 1.0625 keeps the
+// absolute error of lg2 small next to the result.  For e < 1/16 the Taylor series
+// log1p(e) = e - e²/2 + e³/3 - e⁴/4 + ..., truncated after e⁴, errs by less than e⁵/5 ≤ 2e-7·e.
+__device__ __forceinline__ float softplus_fast(float x) {
+  const float e = ex2_approx(-fabsf(x) * kLog2e);
+  const float big = lg2_approx(1.f + e) * kLn2;
+  const float small = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.33333334f), -0.5f), 1.f);
+  return fmaxf(x, 0.f) + (e >= 0.0625f ? big : small);
+}
+
+// silu(z) = z / (1 + e^{-z}); the reciprocal of +inf is 0, so very negative z gives -0.
+__device__ __forceinline__ float silu_fast(float z) { return z * rcp_approx(1.f + ex2_approx(-z * kLog2e)); }
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// Element-wise fp32 arithmetic on float2 pairs as packed fp32x2 instructions (one instruction for two
+// independent operations).
+__device__ __forceinline__ float2 fma2s(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2s(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2s(float2 a, float2 b) { return __fadd2_rn(a, b); }
+
+// ---- raw lane segments: the 2H inputs of one lane, as 16-byte vectors per half -------------------
+// Elements are unpacked with shifts and masks on 32-bit words (a bf16 is the top half of an fp32),
+// never through a local array, so everything stays in registers.
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int w) {
+  return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ float elem_of(const uint4& v, int k, float) { return __uint_as_float(word(v, k)); }
+__device__ __forceinline__ float elem_of(const uint4& v, int k, __nv_bfloat16) {
+  const uint32_t w = word(v, k >> 1);
+  return __uint_as_float((k & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+__device__ __forceinline__ uint32_t raw_bits(const float* p, int64_t i) { return __float_as_uint(p[i]); }
+__device__ __forceinline__ uint32_t raw_bits(const __nv_bfloat16* p, int64_t i) {
+  return reinterpret_cast<const unsigned short*>(p)[i];
+}
+__device__ __forceinline__ uint32_t out_bits(float v, float) { return __float_as_uint(v); }
+__device__ __forceinline__ uint32_t out_bits(float v, __nv_bfloat16) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+template <typename T, int H>
+struct Seg {
+  static constexpr int kPerVec = 16 / sizeof(T);
+  static constexpr int kVecs = H / kPerVec;
+  static_assert(H % kPerVec == 0, "a half-segment must be whole 16-byte vectors");
+  uint4 v[2][kVecs];
+  __device__ __forceinline__ float get(int half, int i) const { return elem_of(v[half][i / kPerVec], i % kPerVec, T()); }
+};
+
+// Load steps [t, t+2H) of a row (length L) as two halves.  Steps at or past L read as 0.
+template <typename T, int H>
+__device__ __forceinline__ void load_seg(Seg<T, H>& s, const T* __restrict__ row, int64_t t, int64_t L, bool vec) {
+  constexpr int kPerVec = Seg<T, H>::kPerVec;
+  if (vec && t + 2 * H <= L) {
+#pragma unroll
+    for (int h = 0; h < 2; h++)
+#pragma unroll
+      for (int q = 0; q < Seg<T, H>::kVecs; q++)
+        s.v[h][q] = __ldg(reinterpret_cast<const uint4*>(row + t + h * H) + q);
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; h++)
+#pragma unroll
+      for (int q = 0; q < Seg<T, H>::kVecs; q++) {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int k = 0; k < kPerVec; k++) {
+          const int64_t tt = t + h * H + q * kPerVec + k;
+          const uint32_t bits = tt < L ? raw_bits(row, tt) : 0u;
+          if (sizeof(T) == 4) w[k] = bits;
+          else w[k >> 1] |= (k & 1) ? (bits << 16) : bits;
+        }
+        s.v[h][q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+  }
+}
+
+template <typename T, int H>
+__device__ __forceinline__ void store_seg(T* __restrict__ row, int64_t t, int64_t L, bool vec, const float2 (&y)[H]) {
+  constexpr int kPerVec = 16 / sizeof(T);
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    if (vec && t + 2 * H <= L) {
+#pragma unroll
+      for (int q = 0; q < H / kPerVec; q++) {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int k = 0; k < kPerVec; k++) {
+          const float2 v = y[q * kPerVec + k];
+          const uint32_t bits = out_bits(h ? v.y : v.x, T());
+          if (sizeof(T) == 4) w[k] = bits;
+          else w[k >> 1] |= (k & 1) ? (bits << 16) : bits;
+        }
+        reinterpret_cast<uint4*>(row + t + h * H)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < H; i++) {
+        const int64_t tt = t + h * H + i;
+        if (tt < L) row[tt] = from_f32<T>(h ? y[i].y : y[i].x);
+      }
+    }
+  }
+}
+
+// ---- mbarrier / bulk-copy primitives ------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if the phase did not complete within kWaitLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (long long i = 0; i < kWaitLimit; i++)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// 2-D tiled copy of the box at (x, y) (x: innermost coordinate, in elements) of a tensor map.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+
+}  // namespace selscan

@@ -1,0 +1,105 @@
+// Recurrent decode step: one token per (batch, channel) row, state updated in place.
+//
+//   Δ = softplus(δ + Δ_bias[d]),  h[n] ← exp(Δ A[d,n]) h[n] + Δ B[b,n] u,
+//   y = Σ_n C[b,n] h[n] + D[d] u,  out = y silu(z)
+// This is the recurrent (RNN-mode) form of the selective scan with a constant-size state
+// ("Mamba架构深度剖析：如何以线性时间重塑序列建模" §3; recurrence from "Mamba状态空间模型深度解析"
+// §2.1).  It is a streaming read-modify-write of the fp32 state [B, D, N]: Q = NS/4 consecutive
+// threads share one row, each owning four states (one 16-byte vector), so a warp reads and writes
+// 512 contiguous bytes of state per access.  The Q partial sums of y meet with shuffles.
+#include "selscan_internal.cuh"
+
+namespace selscan {
+namespace {
+
+template <int NS, typename Tin, typename Tout>
+__global__ void __launch_bounds__(256) selscan_step_kernel(const StepParams p) {
+  constexpr int Q = NS / 4;  // threads per row
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t rows = p.batch * p.dim;
+  const int64_t row = gid / Q;
+  const int q = static_cast<int>(gid % Q);
+  const bool ok = row < rows;  // whole rows are in or out together (Q divides 32)
+  const int N = p.dstate;
+  const int64_t b = ok ? row / p.dim : 0;
+  const int64_t d = ok ? row - b * p.dim : 0;
+
+  float y = 0.f, uu = 0.f;
+  if (ok) {
+    uu = to_f32(static_cast<const Tin*>(p.u)[row]);
+    const float x = to_f32(static_cast<const Tin*>(p.delta)[row]) + (p.delta_bias ? p.delta_bias[d] : 0.f);
+    const float dt = p.delta_softplus ? softplus_f(x) : x;
+    const float du = dt * uu;
+    const Tin* Bb = static_cast<const Tin*>(p.B) + b * N;
+    const Tin* Cb = static_cast<const Tin*>(p.C) + b * N;
+    float h[4], a[4];
+    float* st = p.state + row * N + 4 * q;
+    const float* Ar = p.A + d * N + 4 * q;
+    const bool vec = p.vec_state && 4 * q + 4 <= N;  // all four of this thread's states exist
+    if (vec) {
+      const float4 hv = __ldcs(reinterpret_cast<const float4*>(st));
+      const float4 av = __ldg(reinterpret_cast<const float4*>(Ar));
+      h[0] = hv.x; h[1] = hv.y; h[2] = hv.z; h[3] = hv.w;
+      a[0] = av.x; a[1] = av.y; a[2] = av.z; a[3] = av.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const bool in = 4 * q + j < N;
+        h[j] = in ? st[j] : 0.f;
+        a[j] = in ? Ar[j] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const int n = 4 * q + j;
+      if (n < N) {
+        h[j] = fmaf(ex2_approx(dt * a[j] * kLog2e), h[j], du * to_f32(Bb[n]));
+        y = fmaf(to_f32(Cb[n]), h[j], y);
+      }
+    }
+    if (vec) {
+      __stcs(reinterpret_cast<float4*>(st), make_float4(h[0], h[1], h[2], h[3]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        if (4 * q + j < N) st[j] = h[j];
+    }
+  }
+  // Sum the Q partial dot products of the row (lanes of a row are adjacent in the warp).
+#pragma unroll
+  for (int o = 1; o < Q; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+  if (ok && q == 0) {
+    y = fmaf(p.D ? p.D[d] : 0.f, uu, y);
+    if (p.z) y *= silu_f(to_f32(static_cast<const Tin*>(p.z)[row]));
+    static_cast<Tout*>(p.out)[row] = from_f32<Tout>(y);
+  }
+}
+
+template <int NS, typename Tin, typename Tout>
+cudaError_t launch_ns(const StepParams& p, cudaStream_t s) {
+  constexpr int Q = NS / 4;
+  const int64_t threads = p.batch * p.dim * Q;
+  const int block = 256;
+  const int64_t grid = (threads + block - 1) / block;
+  selscan_step_kernel<NS, Tin, Tout><<<static_cast<unsigned>(grid), block, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t dispatch_ns(const StepParams& p, cudaStream_t s) {
+  if (p.dstate <= 4) return launch_ns<4, Tin, Tout>(p, s);
+  if (p.dstate <= 8) return launch_ns<8, Tin, Tout>(p, s);
+  return launch_ns<16, Tin, Tout>(p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_step(const StepParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s) {
+  if (in_dtype == SELSCAN_F32) {
+    return out_dtype == SELSCAN_F32 ? dispatch_ns<float, float>(p, s) : dispatch_ns<float, __nv_bfloat16>(p, s);
+  }
+  return out_dtype == SELSCAN_F32 ? dispatch_ns<__nv_bfloat16, float>(p, s)
+                                  : dispatch_ns<__nv_bfloat16, __nv_bfloat16>(p, s);
+}
+
+}  // namespace selscan

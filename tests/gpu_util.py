@@ -1,0 +1,109 @@
+"""Helpers for GPU-vs-oracle parity tests: numpy inputs -> CUDA tensors -> libselscan -> numpy."""
+from __future__ import annotations
+
+import numpy as np
+
+FP32_TOL = (1e-4, 1e-4)  # fp32 inputs: |out - ref| <= 1e-4 + 1e-4·|ref|
+BF16_TOL = (2e-3, 2e-3)  # bf16 inputs, fp32 state: |out - ref| <= 2e-3 + 2e-3·|ref|
+H_RTOL = 1e-4  # h_last: |h - ref| <= 1e-4 · max_n |ref[b, d, :]|, relative to each channel's state vector
+
+
+def to_dev(a, in_dtype=None, device="cuda"):
+    """numpy -> torch CUDA tensor; uint16 arrays are bf16 bit patterns."""
+    import torch
+
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def gpu_fwd(inp, delta_softplus=True, out_dtype="f32", h_last=True, stream=None, **over):
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    t.update(over)
+    od = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    out, hl = ss.selscan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                             delta_bias=t["delta_bias"], delta_softplus=delta_softplus, h0=t["h0"], out_dtype=od,
+                             return_h_last=h_last, stream=stream)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64), (None if hl is None else hl.cpu().numpy().astype(np.float64))
+
+
+def tol_for(in_dtype):
+    return FP32_TOL if in_dtype == "f32" else BF16_TOL
+
+
+def check_out(got, ref, in_dtype, what="out", extra_rel=0.0):
+    atol, rtol = tol_for(in_dtype)
+    err = np.abs(got - ref)
+    bound = atol + (rtol + extra_rel) * np.abs(ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = int(np.argmax(np.where(bad, err - bound, -np.inf)))
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; worst at flat {i}: "
+                             f"got {got.flat[i]!r} ref {ref.flat[i]!r} (max err {err.max():.3e})")
+    return float(err.max())
+
+
+def check_h(got, ref, what="h_last"):
+    """Relative error of each channel's final state vector in the max norm over its N states.
+
+    A state entry near zero is the difference of terms as large as the vector's largest entry, so its
+    fp32 error is set by that scale; the bound is therefore relative to max_n |ref| of the channel.
+    """
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    scale = np.max(np.abs(ref), axis=-1, keepdims=True)
+    err = np.abs(got - ref)
+    bound = H_RTOL * np.broadcast_to(scale, ref.shape)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = int(np.argmax(np.where(bad, err - bound, -np.inf)))
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; worst at flat {i}: "
+                             f"got {got.flat[i]!r} ref {ref.flat[i]!r} "
+                             f"(channel scale {np.broadcast_to(scale, ref.shape).flat[i]:.3e})")
+    return float(np.max(err / np.maximum(np.broadcast_to(scale, ref.shape), 1e-300)))
+
+
+def sample_rows(Bsz, Dm, k, seed=0):
+    """k flat row indices b*D + d, always including the first and last row."""
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(Bsz * Dm, size=min(k, Bsz * Dm), replace=False).tolist())
+    rows.update({0, Bsz * Dm - 1})
+    return sorted(rows)
+
+
+def decode_as_sequences(inp, rows):
+    """Rearrange a decode input ([T, B, D] / [T, B, N]) into forward problems over its steps.
+
+    Returns one forward input dict of shape (1, 1, T, N) per listed flat row
+    b*D + d: the row's T decode steps become a length-T sequence.  T decode
+    steps carrying the state equal the forward over those T steps (an oracle
+    pin), so the oracle can check sampled rows of a full-size decode run.
+    """
+    T = inp["steps"]
+    Bsz, Dm, _, N = inp["shape"]
+    out = []
+    for r in rows:
+        b, d = divmod(r, Dm)
+        case = {"shape": (1, 1, T, N), "in_dtype": inp["in_dtype"], "steps": 0,
+                "u": np.ascontiguousarray(inp["u"][:, b, d]).reshape(1, 1, T),
+                "delta": np.ascontiguousarray(inp["delta"][:, b, d]).reshape(1, 1, T),
+                "z": None if inp.get("z") is None else np.ascontiguousarray(inp["z"][:, b, d]).reshape(1, 1, T),
+                "B": np.ascontiguousarray(inp["B"][:, b, :].T).reshape(1, N, T),
+                "C": np.ascontiguousarray(inp["C"][:, b, :].T).reshape(1, N, T),
+                "A": np.ascontiguousarray(inp["A"][d:d + 1]),
+                "D": None if inp.get("D") is None else np.ascontiguousarray(inp["D"][d:d + 1]),
+                "delta_bias": None if inp.get("delta_bias") is None else
+                np.ascontiguousarray(inp["delta_bias"][d:d + 1]),
+                "h0": None if inp.get("h0") is None else np.ascontiguousarray(inp["h0"][b, d]).reshape(1, 1, N)}
+        out.append(case)
+    return out

@@ -1,0 +1,265 @@
+"""libselscan on the GPU against the fp64 oracle, element by element on the same seeded inputs.
+
+Tolerances (written here, derived from the required accuracy of the scan):
+  fp32 inputs:            |out - ref| <= 1e-4 + 1e-4·|ref|
+  bf16 inputs, fp32 state: |out - ref| <= 2e-3 + 2e-3·|ref|
+  h_last:                 |h - ref| <= 1e-4 · max_n |ref| of the channel (relative, in the max norm
+                          of each channel's state vector)
+Full-size workloads are compared on sampled rows that the oracle computes
+one by one; small shapes (ragged L, odd dstate, channel counts that do not
+fill a CTA) are compared in full.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from gpu_util import (check_h, check_out, decode_as_sequences, gpu_fwd, sample_rows, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+# Both forward kernels: "seq" walks each row sequentially (rows spread over lanes), "chunk" splits
+# each row's sequence over lanes and joins them with a scan.  The library picks by shape; the tests
+# force each one through the SELSCAN_KERNEL override.
+KERNELS = ["seq", "chunk"]
+
+
+@pytest.fixture(params=KERNELS)
+def kernel(request, monkeypatch):
+    monkeypatch.setenv("SELSCAN_KERNEL", request.param)
+    return request.param
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import selective_state_space_152_b300 as ss
+
+    ss.load_library()  # fails loudly if the library was not built
+
+
+def test_tiny_fp32_workload_full(kernel):
+    w = si.WORKLOADS["tiny_fp32"]
+    inp = si.make_inputs(w)
+    ref, href = oracle.selscan_fwd(inp)
+    got, hl = gpu_fwd(inp)
+    check_out(got, ref, "f32")
+    check_h(hl, href)
+
+
+SMALL = [
+    # (seed, B, D, L, N, dtype, z, D, bias, h0, softplus)
+    (1, 1, 1, 1, 1, "f32", True, True, True, True, True),
+    (2, 2, 3, 7, 3, "f32", True, True, True, True, True),
+    (3, 1, 5, 33, 4, "f32", False, True, True, False, True),
+    (4, 2, 9, 255, 5, "f32", True, False, False, True, True),
+    (5, 1, 4, 512, 8, "f32", True, True, True, True, False),
+    (6, 2, 6, 513, 16, "f32", True, True, True, True, True),
+    (7, 3, 7, 1000, 16, "bf16", True, True, True, True, True),
+    (8, 1, 3, 1537, 2, "bf16", False, False, True, True, True),
+    (9, 2, 5, 2048, 16, "bf16", True, True, True, False, True),
+    (10, 1, 2, 4099, 12, "f32", True, True, True, True, True),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"s{c[0]}_B{c[1]}D{c[2]}L{c[3]}N{c[4]}_{c[5]}" for c in SMALL])
+def test_small_shapes_full(case, kernel):
+    seed, Bsz, Dm, L, N, dt, hz, hD, hb, hh, sp = case
+    inp = si.random_case(seed, Bsz, Dm, L, N, in_dtype=dt, has_z=hz, has_D=hD, has_bias=hb, has_h0=hh)
+    if not sp:  # without softplus Δ = δ + bias must stay positive, else Ā > 1 and the state overflows
+        inp["delta_bias"] = None
+        d = np.abs(si.bf16_bits_to_f32(inp["delta"]) if dt == "bf16" else inp["delta"]) * 0.05
+        inp["delta"] = si.f32_to_bf16_bits(d) if dt == "bf16" else d.astype(np.float32)
+    ref, href = oracle.selscan_fwd(inp, delta_softplus=sp)
+    got, hl = gpu_fwd(inp, delta_softplus=sp)
+    check_out(got, ref, dt)
+    check_h(hl, href)
+
+
+@pytest.mark.parametrize("name", ["mamba130m_layer", "long_seq_65k", "width_2p8b"])
+def test_workload_sampled_rows(name):
+    w = si.WORKLOADS[name]
+    inp = si.make_inputs(w)
+    Bsz, Dm, L, N = inp["shape"]
+    got, hl = gpu_fwd(inp)
+    rows = sample_rows(Bsz, Dm, 12 if L > 10000 else 48, seed=len(name))
+    ref, href = oracle.selscan_fwd(inp, rows=rows)
+    check_out(got.reshape(Bsz * Dm, L)[rows], ref, w.in_dtype, what=f"{name} out")
+    check_h(hl.reshape(Bsz * Dm, N)[rows], href, what=f"{name} h_last")
+
+
+def test_bf16_output(kernel):
+    inp = si.random_case(21, 2, 5, 700, 16, in_dtype="bf16")
+    ref, _ = oracle.selscan_fwd(inp)
+    got, _ = gpu_fwd(inp, out_dtype="bf16")
+    # bf16 rounding of the output adds up to 2^-8 relative on top of the bf16-input tolerance
+    check_out(got, ref, "bf16", extra_rel=2.0 ** -8)
+
+
+def test_carry_across_calls(kernel):
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    inp = si.random_case(31, 2, 6, 1500, 16, in_dtype="f32")
+    ref, href = oracle.selscan_fwd(inp)
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    outs = []
+    h = t["h0"].clone()
+    for a, b in [(0, 1), (1, 700), (700, 1100), (1100, 1500)]:
+        sl = {k: t[k][..., a:b].contiguous() for k in ("u", "delta", "z", "B", "C")}
+        o, _ = ss.selscan_fwd(sl["u"], sl["delta"], t["A"], sl["B"], sl["C"], D=t["D"], z=sl["z"],
+                              delta_bias=t["delta_bias"], h0=h, h_last=h)  # in-place carry: h_last aliases h0
+        outs.append(o)
+    torch.cuda.synchronize()
+    got = torch.cat(outs, dim=-1).cpu().numpy().astype(np.float64)
+    check_out(got, ref, "f32", what="chunked-call out")
+    check_h(h.cpu().numpy().astype(np.float64), href, what="chunked-call h_last")
+
+
+def test_decode_step_workload_sampled():
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    w = si.WORKLOADS["decode_step"]
+    inp = si.make_inputs(w, steps=16)  # full batch and width, 16 of the 64 steps
+    Bsz, Dm, _, N = inp["shape"]
+    T = inp["steps"]
+    dev = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    state = dev["h0"].clone()
+    outs = []
+    for s in range(T):
+        o = ss.selscan_step(dev["u"][s], dev["delta"][s], dev["A"], dev["B"][s], dev["C"][s], state, D=dev["D"],
+                            z=dev["z"][s], delta_bias=dev["delta_bias"])
+        outs.append(o)
+    torch.cuda.synchronize()
+    got = torch.stack(outs).cpu().numpy().astype(np.float64)  # [T, B, D]
+    hs = state.cpu().numpy().astype(np.float64)
+    rows = sample_rows(Bsz, Dm, 64, seed=5)
+    for r, case in zip(rows, decode_as_sequences(inp, rows)):
+        b, d = divmod(r, Dm)
+        ref, href = oracle.selscan_fwd(case, nthreads=1)
+        check_out(got[:, b, d], ref[0, 0], "bf16", what=f"decode row {r}")
+        check_h(hs[b, d], href[0, 0], what=f"decode state row {r}")
+
+
+def test_step_small_fp32_odd_dstate():
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    for N in (1, 3, 4, 6, 16):
+        inp = si.random_case(40 + N, 3, 5, 9, N, in_dtype="f32")
+        ref, href = oracle.selscan_fwd(inp)
+        t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+        state = t["h0"].clone()
+        outs = []
+        for s in range(9):
+            outs.append(ss.selscan_step(t["u"][..., s].contiguous(), t["delta"][..., s].contiguous(), t["A"],
+                                        t["B"][..., s].contiguous(), t["C"][..., s].contiguous(), state, D=t["D"],
+                                        z=t["z"][..., s].contiguous(), delta_bias=t["delta_bias"]))
+        torch.cuda.synchronize()
+        got = torch.stack(outs, dim=-1).cpu().numpy().astype(np.float64)
+        check_out(got, ref, "f32", what=f"step N={N}")
+        check_h(state.cpu().numpy().astype(np.float64), href, what=f"step state N={N}")
+
+
+def test_causality_bitwise(kernel):
+    inp = si.random_case(51, 1, 4, 1200, 16, in_dtype="bf16")
+    base, _ = gpu_fwd(inp)
+    for t0 in (0, 511, 512, 777, 1199):
+        p = dict(inp)
+        u = si.bf16_bits_to_f32(inp["u"]).copy()
+        u[..., t0] += 1.0
+        p["u"] = si.f32_to_bf16_bits(u)
+        got, _ = gpu_fwd(p)
+        assert np.array_equal(got[..., :t0], base[..., :t0]), f"outputs before t0={t0} changed"
+
+
+def test_delta_to_zero_limit(kernel):
+    inp = si.random_case(61, 1, 3, 300, 8, in_dtype="f32", has_z=False, has_h0=False)
+    inp["delta_bias"] = np.full(3, -40.0, dtype=np.float32)
+    got, hl = gpu_fwd(inp)
+    want = np.asarray(inp["D"], np.float64)[None, :, None] * np.asarray(inp["u"], np.float64)
+    check_out(got, want, "f32", what="Δ→0 gives D·u")
+    assert np.max(np.abs(hl)) < 1e-12
+
+
+def test_extreme_values(kernel):
+    inp = si.random_case(71, 2, 3, 400, 16, in_dtype="f32")
+    rng = np.random.default_rng(72)
+    inp["delta"] = (rng.standard_normal(inp["delta"].shape) * 30).astype(np.float32)  # softplus far on both sides
+    inp["z"] = (rng.standard_normal(inp["z"].shape) * 60).astype(np.float32)  # gate saturates and underflows
+    ref, href = oracle.selscan_fwd(inp)
+    got, hl = gpu_fwd(inp)
+    check_out(got, ref, "f32")
+    check_h(hl, href)
+
+
+def test_empty_and_zero_length():
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    inp = si.random_case(81, 2, 3, 0, 4, in_dtype="f32")
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    hl = torch.full_like(t["h0"], 7.0)
+    ss.selscan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"], h0=t["h0"], h_last=hl)
+    torch.cuda.synchronize()
+    assert torch.equal(hl, t["h0"]), "L = 0 must pass h0 through"
+    hl2 = torch.full_like(t["h0"], 7.0)
+    ss.selscan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], h_last=hl2)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(hl2) == 0, "L = 0 without h0 gives a zero state"
+    e = torch.empty(0, 3, 5, device="cuda")
+    out, _ = ss.selscan_fwd(e, e, t["A"], torch.empty(0, 4, 5, device="cuda"), torch.empty(0, 4, 5, device="cuda"))
+    assert out.shape == (0, 3, 5)
+
+
+def test_host_side_rejections():
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    inp = si.random_case(91, 1, 4, 64, 4, in_dtype="f32")
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    # output aliasing an input
+    with pytest.raises(ss.SelscanError) as e:
+        ss.selscan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], out=t["u"])
+    assert e.value.status == 7
+    # a tensor whose stated extent runs past the end of its allocation: a 4 MiB cudaMalloc (not the
+    # caching allocator, whose segments can be larger), with u placed 40 bytes before its end while
+    # the shape needs 1 KiB.  The call must be refused before any launch.
+    import ctypes
+
+    lib = ss.load_library()
+    shape = ss.SelscanShape(1, 4, 64, 4, 0, 0)
+    out = torch.empty(1, 4, 64, device="cuda")
+    torch.cuda.synchronize()
+    cudart = ctypes.CDLL("libcudart.so.13")
+    buf = ctypes.c_void_p()
+    assert cudart.cudaMalloc(ctypes.byref(buf), ctypes.c_size_t(4 << 20)) == 0
+    try:
+        tail = buf.value + (4 << 20) - 40
+        st = lib.selscan_fwd(ctypes.byref(shape), tail, t["delta"].data_ptr(), t["A"].data_ptr(),
+                             t["B"].data_ptr(), t["C"].data_ptr(), None, None, None, 1, None, out.data_ptr(), None,
+                             None)
+        assert st == 6, ss.selscan_status_string(st)
+        # the same call with u at the start of the allocation is accepted
+        assert cudart.cudaMemset(buf, 0, ctypes.c_size_t(4 << 20)) == 0
+        st = lib.selscan_fwd(ctypes.byref(shape), buf.value, t["delta"].data_ptr(), t["A"].data_ptr(),
+                             t["B"].data_ptr(), t["C"].data_ptr(), None, None, None, 1, None, out.data_ptr(), None,
+                             None)
+        assert st == 0
+        torch.cuda.synchronize()
+    finally:
+        cudart.cudaFree(buf)
+    # host memory that the device cannot reach
+    host = np.zeros(4 * 64, np.float32)
+    st = lib.selscan_fwd(ctypes.byref(shape), host.ctypes.data, t["delta"].data_ptr(), t["A"].data_ptr(),
+                         t["B"].data_ptr(), t["C"].data_ptr(), None, None, None, 1, None, out.data_ptr(), None, None)
+    assert st == 6
+    torch.cuda.synchronize()
