@@ -127,6 +127,17 @@ def aggregate(elements_per_rank, seconds_per_rank):
     return sum(elements_per_rank) / max(seconds_per_rank)
 
 
+def max_over_ranks(seconds, dist, device):
+    """The largest of the ranks' times (the job's time); the value itself when not distributed."""
+    if dist is None:
+        return seconds
+    import torch
+
+    tt = torch.tensor([float(seconds)], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_152_b300", "csrc")
@@ -313,11 +324,7 @@ def run_ours(args, rank, world, local_rank, dist):
     torch.cuda.synchronize()
     step_s = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
     t_sum = sum(step_s)
-    t_max = t_sum
-    if dist is not None:
-        tt = torch.tensor([t_sum], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(t_sum, dist, device)
     elems_rank = Bsz * Dm * L * args.steps
     value = elems_rank * world / t_max
 
@@ -388,11 +395,7 @@ def run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world):
         one()
     ev1.record(stream)
     torch.cuda.synchronize()
-    secs = ev0.elapsed_time(ev1) / 1e3
-    if dist is not None:
-        tt = torch.tensor([secs], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        secs = float(tt.item())
+    secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist, device)
     return {"value": Bsz * Dm * L * steps * world / secs, "unit": "elems/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": secs / steps * 1e3,
             "gpu_launches": steps}
