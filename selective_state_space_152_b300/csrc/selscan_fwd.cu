@@ -24,12 +24,17 @@
 // The end state of the chunk is carried in registers into the next chunk, so long sequences never
 // write their state to memory.
 //
-// B and C of a chunk are shared by every channel of the CTA.  They are fetched by the tensor
-// memory accelerator (1-D bulk copies, double-buffered one chunk ahead) as raw rows, then widened
-// once per CTA to fp32 in a layout where one 128-bit shared load yields the float2 pairs of two
-// consecutive steps.  Steps past the end of the sequence get Δ = 0 and u = 0: the identity pair
-// (1, 0), so a ragged last chunk needs no special case in the scan.
+// Staging.  One thread issues the tensor-memory-accelerator copies of chunk c+1 while chunk c is
+// computed (two buffers): u, δ and z of the CTA's channels as 2-D tiles [ROWS][T] with the 128-byte
+// swizzle (each lane then reads its K steps as 16-byte shared loads), and the raw B, C rows of the
+// batch entry.  Where the tensor copies cannot be used (rows not 16-byte aligned, channel blocks not
+// a multiple of 8, or a chunk narrower than a 128-byte row) the lanes read u, δ, z from global
+// memory and B, C come by 1-D bulk copies or plain loads.  B and C are shared by every channel of
+// the CTA; they are widened once per CTA to fp32 in a layout where one 128-bit shared load yields
+// the float2 pairs of two consecutive steps.  Steps past the end of the sequence get Δ = 0 and u = 0:
+// the identity pair (1, 0), so a ragged last chunk needs no special case in the scan.
 #include <cstdlib>
+#include <cstring>
 
 #include "selscan_internal.cuh"
 
@@ -39,6 +44,13 @@ namespace selscan {
 __device__ int g_selscan_device_error = 0;
 
 namespace {
+
+// SELSCAN_STAGING=0 makes the chunked kernel read u, δ, z from global memory even where the tensor
+// copies could be used (for tuning and for testing the direct path on aligned inputs).
+bool staging_disabled() {
+  const char* e = getenv("SELSCAN_STAGING");
+  return e && e[0] == '0';
+}
 
 // ---- the kernel ----------------------------------------------------------------------------------
 
@@ -55,26 +67,55 @@ struct Cfg {
   static constexpr int RAW = 2 * NS * T;     // raw elements of one chunk (B rows then C rows)
   static constexpr int UNITS = 2 * NS * P;   // widening work units per chunk (tensor, n, lane segment)
   static constexpr int UNITS_PER_THREAD = (UNITS + R * 32 - 1) / (R * 32);
+  static constexpr int EPR = 128 / static_cast<int>(sizeof(Tin));  // inputs per 128-byte stage row
+  // Tensor copies of u, δ, z need whole 128-byte stage rows and boxes of whole 1 KiB swizzle atoms.
+  static constexpr bool kTmaShape = T % EPR == 0 && ROWS % 8 == 0;
+  static constexpr int SUBT = kTmaShape ? T / EPR : 1;                  // boxes per tensor per chunk
+  static constexpr int BCX = T < 128 ? T : 128;                         // steps per B / C box
+  static constexpr int NB = T / BCX;                                    // B (and C) boxes per chunk
+  static constexpr size_t kStageTensor = static_cast<size_t>(ROWS) * T * sizeof(Tin);
+  static constexpr size_t kStageBytes = kTmaShape ? 2 * 3 * kStageTensor : 0;  // double-buffered u, δ, z
   static constexpr size_t kTileBytes = 2 * TILE * sizeof(float);  // double-buffered
   static constexpr size_t kRawBytes = 2 * RAW * sizeof(Tin);       // double-buffered
-  static constexpr size_t kSmem = kTileBytes + kRawBytes + 2 * sizeof(uint64_t);
+  static constexpr size_t kSmem = 1024 + kStageBytes + kTileBytes + kRawBytes + 2 * sizeof(uint64_t);
   static_assert(K % 4 == 0 && P >= 1 && P <= 32 && 32 % P == 0, "bad tile shape");
+  static_assert(T % BCX == 0, "B, C boxes must tile the chunk");
 };
 
+// K consecutive inputs [e0, e0 + K) of stage row r of one tensor's stage [SUBT][ROWS][EPR], as two
+// halves.  The stage was written by a 2-D tensor copy with the 128-byte swizzle: 16-byte chunk c of
+// the stage row at byte offset 128·q sits at chunk position c ^ (q mod 8).
+template <typename Tin, int H, int ROWS>
+__device__ __forceinline__ void load_seg_stage(Seg<Tin, H>& s, const unsigned char* __restrict__ stage, int r,
+                                               int e0) {
+  constexpr int kPerVec = Seg<Tin, H>::kPerVec, EPR = 128 / static_cast<int>(sizeof(Tin));
+#pragma unroll
+  for (int h = 0; h < 2; h++)
+#pragma unroll
+    for (int q = 0; q < Seg<Tin, H>::kVecs; q++) {
+      const int e = e0 + h * H + q * kPerVec;
+      const int srow = (e / EPR) * ROWS + r, chunk = (e % EPR) / kPerVec;
+      s.v[h][q] = *reinterpret_cast<const uint4*>(stage + srow * 128 + ((chunk ^ (srow & 7)) << 4));
+    }
+}
+
 // Widen raw chunk c (raw buffer rb) into tile buffer tb.  MASK: zero steps at or past L and states
-// at or past N (the raw buffer holds stale data there).
-template <int NS, int P, int K, int R, typename Tin, bool MASK>
+// at or past N (the raw buffer holds stale data there).  The raw chunk is [2 tensors][NB][NS][BCX]
+// as written by the tensor copies (BOXED), else [2 tensors][NS][T].
+template <int NS, int P, int K, int R, typename Tin, bool MASK, bool BOXED>
 __device__ __forceinline__ void widen(const Tin* __restrict__ rb, float* __restrict__ tb, int tid, int64_t t0,
                                       int64_t L, int N) {
   using C = Cfg<NS, P, K, R, Tin>;
   constexpr int H = C::H;
+  constexpr int BX = BOXED ? C::BCX : C::T;
 #pragma unroll
   for (int k = 0; k < C::UNITS_PER_THREAD; k++) {
     const int unit = tid + k * R * 32;
     if (C::UNITS % (R * 32) != 0 && unit >= C::UNITS) break;
     const int s = unit % P, rowi = unit / P;  // rowi = tensor * NS + n
     Seg<Tin, H> rs;
-    const uint4* src = reinterpret_cast<const uint4*>(rb + rowi * C::T + s * K);
+    const int tensor = rowi / NS, n_raw = rowi % NS, box = (s * K) / BX, x = (s * K) % BX;
+    const uint4* src = reinterpret_cast<const uint4*>(rb + tensor * NS * C::T + (box * NS + n_raw) * BX + x);
 #pragma unroll
     for (int h = 0; h < 2; h++)
 #pragma unroll
@@ -107,19 +148,29 @@ struct Carry {
 
 // One chunk for one lane: inputs, then the states in groups of G, then the gated output.
 // TAIL: the chunk runs past L or rows are not 16-byte aligned (masked, scalar-safe loads and stores).
-template <int NS, int P, int K, int G, typename Tin, typename Tout, bool FULLN, bool TAIL, bool SOFTPLUS>
+// STAGED: u, δ, z come from the chunk's shared-memory stage [3][SUBT][ROWS][128 B] (row r_local,
+// inputs [jK, jK + K)); otherwise from global memory.
+template <int NS, int P, int K, int G, int ROWS, typename Tin, typename Tout, bool FULLN, bool TAIL, bool SOFTPLUS,
+          bool STAGED>
 __device__ __forceinline__ void compute_chunk(const FwdParams& p, Carry<NS>& cs, const float* __restrict__ tb,
                                               int j, int rw, int64_t ts, int64_t L, float bias, float Dd,
                                               const Tin* __restrict__ u_row, const Tin* __restrict__ dl_row,
-                                              const Tin* __restrict__ z_row, Tout* __restrict__ o_row, bool row_ok) {
+                                              const Tin* __restrict__ z_row, Tout* __restrict__ o_row, bool row_ok,
+                                              const unsigned char* __restrict__ stage, size_t stage_tensor,
+                                              int r_local) {
   constexpr int H = K / 2, KP = K + 4, SEG = P * KP;
   const int N = FULLN ? NS : p.dstate;
   float2 dl[H], du[H], y[H];
   float S0 = 0.f, S1 = 0.f;  // Σ Δ over each half
   {
     Seg<Tin, H> us, ds;
-    load_seg<Tin, H>(us, u_row, ts, L, !TAIL);
-    load_seg<Tin, H>(ds, dl_row, ts, L, !TAIL);
+    if (STAGED) {
+      load_seg_stage<Tin, H, ROWS>(us, stage, r_local, j * K);
+      load_seg_stage<Tin, H, ROWS>(ds, stage + stage_tensor, r_local, j * K);
+    } else {
+      load_seg<Tin, H>(us, u_row, ts, L, !TAIL);
+      load_seg<Tin, H>(ds, dl_row, ts, L, !TAIL);
+    }
     const float2 bias2 = f2(bias, bias), D2 = f2(Dd, Dd);
 #pragma unroll
     for (int i = 0; i < H; i++) {
@@ -247,7 +298,10 @@ __device__ __forceinline__ void compute_chunk(const FwdParams& p, Carry<NS>& cs,
 
   if (z_row) {
     Seg<Tin, H> zs;
-    load_seg<Tin, H>(zs, z_row, ts, L, !TAIL);
+    if (STAGED)
+      load_seg_stage<Tin, H, ROWS>(zs, stage + 2 * stage_tensor, r_local, j * K);
+    else
+      load_seg<Tin, H>(zs, z_row, ts, L, !TAIL);
 #pragma unroll
     for (int i = 0; i < H; i++) y[i] = mul2s(y[i], f2(silu_fast(zs.get(0, i)), silu_fast(zs.get(1, i))));
   }
@@ -259,16 +313,22 @@ __device__ __forceinline__ void compute_chunk(const FwdParams& p, Carry<NS>& cs,
 #define SELSCAN_WARPS_PER_SM 12
 #endif
 
-template <int NS, int P, int K, int R, int G, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
-__global__ void __launch_bounds__(R * 32, SELSCAN_WARPS_PER_SM / R) selscan_fwd_kernel(const FwdParams p) {
+// STAGED: u, δ, z and B, C arrive by 2-D tensor copies (maps), else as described at the top.
+template <int NS, int P, int K, int R, int G, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS, bool STAGED>
+__global__ void __launch_bounds__(R * 32, SELSCAN_WARPS_PER_SM / R)
+    selscan_fwd_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
   using C = Cfg<NS, P, K, R, Tin>;
   constexpr int T = C::T;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  float* tiles = reinterpret_cast<float*>(smem_raw);                  // [2 buffers][2][NS][P][KP]
-  Tin* raw = reinterpret_cast<Tin*>(smem_raw + C::kTileBytes);         // [2 buffers][2][NS][T]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + C::kTileBytes + C::kRawBytes);
+  // The u, δ, z stage starts on a 1 KiB boundary (the period of the 128-byte swizzle).
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* stage = smem;                                                  // [2 buffers][3][SUBT][ROWS][128 B]
+  float* tiles = reinterpret_cast<float*>(smem + C::kStageBytes);               // [2 buffers][2][NS][P][KP]
+  Tin* raw = reinterpret_cast<Tin*>(smem + C::kStageBytes + C::kTileBytes);     // [2 buffers][RAW]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStageBytes + C::kTileBytes + C::kRawBytes);
   __shared__ int s_abort;
-  __shared__ float s_A2[C::ROWS][NS], s_carry[C::ROWS][NS];
+  // Row stride NS + 1: the RPW channels of a quarter-warp reading state n hit distinct banks.
+  __shared__ float s_A2[C::ROWS][NS + 1], s_carry[C::ROWS][NS + 1];
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -278,39 +338,65 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_WARPS_PER_SM / R) selscan_fwd_
   const int j = lane / C::RPW;  // segment of this lane within its channel
   const int r_local = (tid >> 5) * C::RPW + rw;
   const int64_t b = blockIdx.y;
-  const int64_t d = static_cast<int64_t>(blockIdx.x) * C::ROWS + r_local;
+  const int64_t d0 = static_cast<int64_t>(blockIdx.x) * C::ROWS;
+  const int64_t d = d0 + r_local;
   const bool row_ok = d < p.dim;
   const int N = FULLN ? NS : p.dstate;
   const int64_t L = p.seqlen;
   const int64_t nchunks = (L + T - 1) / T;
   const Tin* __restrict__ Bsrc = static_cast<const Tin*>(p.B) + b * N * L;
   const Tin* __restrict__ Csrc = static_cast<const Tin*>(p.C) + b * N * L;
-  const bool tma = p.vec_bc;
+  const bool bulk = STAGED || p.vec_bc;  // chunks arrive by asynchronous copies (else plain loads)
+  const bool has_z = p.z != nullptr;
 
-  // Issue the raw B, C rows of chunk c into raw buffer c & 1 (one thread).
+  // Issue the copies of chunk c into buffer c & 1 (one thread).
   auto issue = [&](int64_t c) {
     const int64_t t0 = c * T;
-    const int64_t len = (L - t0) < T ? (L - t0) : T;
-    const uint32_t bytes = static_cast<uint32_t>(len * sizeof(Tin));
     Tin* dst = raw + (c & 1) * C::RAW;
+    uint64_t* bar = &bars[c & 1];
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(&bars[c & 1], 2u * N * bytes);
-    for (int n = 0; n < N; n++) {
-      bulk_copy_g2s(dst + n * T, Bsrc + n * L + t0, bytes, &bars[c & 1]);
-      bulk_copy_g2s(dst + (NS + n) * T, Csrc + n * L + t0, bytes, &bars[c & 1]);
+    if (STAGED) {
+      // Whole boxes always land (zero-filled past the tensor), so the byte count is fixed.
+      const uint32_t bytes = static_cast<uint32_t>((has_z ? 3 : 2) * C::kStageTensor +
+                                                   2 * C::NB * NS * C::BCX * sizeof(Tin));
+      mbar_expect_tx(bar, bytes);
+      unsigned char* st = stage + (c & 1) * 3 * C::kStageTensor;
+      const int x0 = static_cast<int>(t0), y0 = static_cast<int>(b * p.dim + d0);
+      const CUtensorMap* m[3] = {&maps.u, &maps.delta, &maps.z};
+#pragma unroll
+      for (int k = 0; k < 3; k++) {
+        if (k == 2 && !has_z) break;
+#pragma unroll
+        for (int sub = 0; sub < C::SUBT; sub++)
+          tma_load_2d(st + k * C::kStageTensor + sub * C::ROWS * 128, m[k], x0 + sub * C::EPR, y0, bar);
+      }
+      const int yb = static_cast<int>(b * N);
+#pragma unroll
+      for (int box = 0; box < C::NB; box++) {
+        tma_load_2d(dst + box * NS * C::BCX, &maps.B, x0 + box * C::BCX, yb, bar);
+        tma_load_2d(dst + NS * T + box * NS * C::BCX, &maps.C, x0 + box * C::BCX, yb, bar);
+      }
+    } else {
+      const int64_t len = (L - t0) < T ? (L - t0) : T;
+      const uint32_t bytes = static_cast<uint32_t>(len * sizeof(Tin));
+      mbar_expect_tx(bar, 2u * N * bytes);
+      for (int n = 0; n < N; n++) {
+        bulk_copy_g2s(dst + n * T, Bsrc + n * L + t0, bytes, bar);
+        bulk_copy_g2s(dst + (NS + n) * T, Csrc + n * L + t0, bytes, bar);
+      }
     }
   };
 
   if (tid == 0) {
     s_abort = 0;
-    if (tma) {
+    if (bulk) {
       mbar_init(&bars[0], 1);
       mbar_init(&bars[1], 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
   }
   __syncthreads();
-  if (tma && tid == 0 && nchunks > 0) issue(0);
+  if (bulk && tid == 0 && nchunks > 0) issue(0);
 
   Carry<NS> cs{s_A2[r_local], s_carry[r_local]};
   if (j == 0) {
@@ -324,12 +410,13 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_WARPS_PER_SM / R) selscan_fwd_
   // (the chunk loop's first barrier orders these writes before any read)
   const float bias = (row_ok && p.delta_bias) ? p.delta_bias[d] : 0.f;
   const float Dd = (row_ok && p.D) ? p.D[d] : 0.f;
-  // Channels past `dim` (tail of the last CTA) run the scan on channel 0's inputs so that every lane
-  // takes part in the warp shuffles; only their stores are skipped.
+  // Channels past `dim` (tail of the last CTA) run the scan on channel 0's inputs (or, staged, on
+  // whatever rows the tile holds there) so that every lane takes part in the warp shuffles; only
+  // their stores are skipped.
   const int64_t row_off = (b * p.dim + (row_ok ? d : 0)) * L;
   const Tin* __restrict__ u_row = static_cast<const Tin*>(p.u) + row_off;
   const Tin* __restrict__ dl_row = static_cast<const Tin*>(p.delta) + row_off;
-  const Tin* __restrict__ z_row = p.z ? static_cast<const Tin*>(p.z) + row_off : nullptr;
+  const Tin* __restrict__ z_row = has_z ? static_cast<const Tin*>(p.z) + row_off : nullptr;
   Tout* __restrict__ o_row = static_cast<Tout*>(p.out) + row_off;
 
   int64_t c = 0;
@@ -338,7 +425,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_WARPS_PER_SM / R) selscan_fwd_
     const Tin* rb = raw + (c & 1) * C::RAW;
     float* tb = tiles + (c & 1) * C::TILE;
     const bool tail = t0 + T > L;
-    if (tma) {
+    if (bulk) {
       if (!mbar_wait(&bars[c & 1], static_cast<uint32_t>((c >> 1) & 1))) s_abort = 1;
     } else {
       // Unaligned or ragged B, C rows: every thread loads part of the raw chunk directly.
@@ -352,21 +439,22 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_WARPS_PER_SM / R) selscan_fwd_
       __syncthreads();
     }
     if (FULLN && !tail)
-      widen<NS, P, K, R, Tin, false>(rb, tb, tid, t0, L, N);
+      widen<NS, P, K, R, Tin, false, STAGED>(rb, tb, tid, t0, L, N);
     else
-      widen<NS, P, K, R, Tin, true>(rb, tb, tid, t0, L, N);
-    // Tile c is complete, and every warp has finished chunk c-1 (whose raw buffer the next copy reuses).
+      widen<NS, P, K, R, Tin, true, STAGED>(rb, tb, tid, t0, L, N);
+    // Tile c is complete, and every warp has finished chunk c-1 (whose buffers the next copy reuses).
     __syncthreads();
     if (s_abort) break;
-    if (tma && tid == 0 && c + 1 < nchunks) issue(c + 1);
+    if (bulk && tid == 0 && c + 1 < nchunks) issue(c + 1);
 
     const int64_t ts = t0 + static_cast<int64_t>(j) * K;  // this lane's first step
+    const unsigned char* st = stage + (c & 1) * 3 * C::kStageTensor;
     if (!tail && p.vec_in && p.vec_out)
-      compute_chunk<NS, P, K, G, Tin, Tout, FULLN, false, SOFTPLUS>(p, cs, tb, j, rw, ts, L, bias, Dd, u_row, dl_row,
-                                                                   z_row, o_row, row_ok);
+      compute_chunk<NS, P, K, G, C::ROWS, Tin, Tout, FULLN, false, SOFTPLUS, STAGED>(
+          p, cs, tb, j, rw, ts, L, bias, Dd, u_row, dl_row, z_row, o_row, row_ok, st, C::kStageTensor, r_local);
     else
-      compute_chunk<NS, P, K, G, Tin, Tout, FULLN, true, SOFTPLUS>(p, cs, tb, j, rw, ts, L, bias, Dd, u_row, dl_row,
-                                                                  z_row, o_row, row_ok);
+      compute_chunk<NS, P, K, G, C::ROWS, Tin, Tout, FULLN, true, SOFTPLUS, STAGED>(
+          p, cs, tb, j, rw, ts, L, bias, Dd, u_row, dl_row, z_row, o_row, row_ok, st, C::kStageTensor, r_local);
   }
 
   if (s_abort) {
@@ -386,16 +474,40 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_WARPS_PER_SM / R) selscan_fwd_
   }
 }
 
-template <int NS, int P, int K, int R, int G, typename Tin, typename Tout, bool FULLN>
-cudaError_t launch_cfg(const FwdParams& p, cudaStream_t s) {
+size_t smem_bytes(int NS, int P, size_t in_bytes);
+
+template <int NS, int P, int K, int R, int G, typename Tin, typename Tout, bool FULLN, bool STAGED>
+cudaError_t launch_kernel(const FwdParams& p, const TmaMaps& maps, cudaStream_t s) {
   using C = Cfg<NS, P, K, R, Tin>;
-  auto kern = p.delta_softplus ? selscan_fwd_kernel<NS, P, K, R, G, Tin, Tout, FULLN, true>
-                               : selscan_fwd_kernel<NS, P, K, R, G, Tin, Tout, FULLN, false>;
+  if (smem_bytes(NS, P, sizeof(Tin)) != C::kSmem) return cudaErrorInvalidConfiguration;  // estimate out of step
+  auto kern = p.delta_softplus ? selscan_fwd_kernel<NS, P, K, R, G, Tin, Tout, FULLN, true, STAGED>
+                               : selscan_fwd_kernel<NS, P, K, R, G, Tin, Tout, FULLN, false, STAGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>((p.dim + C::ROWS - 1) / C::ROWS), static_cast<unsigned>(p.batch));
-  kern<<<grid, R * 32, C::kSmem, s>>>(p);
+  kern<<<grid, R * 32, C::kSmem, s>>>(p, maps);
   return cudaGetLastError();
+}
+
+// The staged kernel when the shape allows tensor copies and the maps encode, else the direct one.
+template <int NS, int P, int K, int R, int G, typename Tin, typename Tout, bool FULLN>
+cudaError_t launch_cfg(const FwdParams& p, cudaStream_t s) {
+  using C = Cfg<NS, P, K, R, Tin>;
+  TmaMaps maps;
+  memset(&maps, 0, sizeof maps);
+  if constexpr (C::kTmaShape) {
+    const EncodeTiled enc = reinterpret_cast<EncodeTiled>(tensor_map_encoder());
+    const uint64_t rows = static_cast<uint64_t>(p.batch * p.dim), bc_rows = static_cast<uint64_t>(p.batch * p.dstate);
+    const uint64_t L = static_cast<uint64_t>(p.seqlen);
+    bool ok = enc && p.vec_stage && p.vec_in && rows < (1ull << 31) && bc_rows < (1ull << 31) && L < (1ull << 31);
+    ok = ok && encode_2d<Tin>(enc, &maps.u, p.u, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_2d<Tin>(enc, &maps.delta, p.delta, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         (!p.z || encode_2d<Tin>(enc, &maps.z, p.z, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+         encode_2d<Tin>(enc, &maps.B, p.B, L, bc_rows, C::BCX, NS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         encode_2d<Tin>(enc, &maps.C, p.C, L, bc_rows, C::BCX, NS, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (ok && !staging_disabled()) return launch_kernel<NS, P, K, R, G, Tin, Tout, FULLN, true>(p, maps, s);
+  }
+  return launch_kernel<NS, P, K, R, G, Tin, Tout, FULLN, false>(p, maps, s);
 }
 
 // Warps per CTA for each lane count: enough channels per CTA (32·R/P) to amortise the per-chunk
@@ -418,16 +530,23 @@ cudaError_t launch_cfg(const FwdParams& p, cudaStream_t s) {
 #ifndef SELSCAN_G
 #define SELSCAN_G 2
 #endif
-constexpr int kK = 16;
+#ifndef SELSCAN_K
+#define SELSCAN_K 16
+#endif
+constexpr int kK = SELSCAN_K;  // steps per lane-segment
 
 // Warps of one CTA of the chunked kernel for P lanes per channel (the table above).
 constexpr int warps_per_cta_for(int P) {
   return P == 2 ? SELSCAN_R_P2 : P == 4 ? SELSCAN_R_P4 : P == 8 ? SELSCAN_R_P8 : P == 16 ? SELSCAN_R_P16 : SELSCAN_R_P32;
 }
 
+// Dynamic shared memory of the kernel for NS states and P lanes (Cfg::kSmem, evaluated at run time).
 size_t smem_bytes(int NS, int P, size_t in_bytes) {
-  const size_t T = static_cast<size_t>(P) * kK;
-  return 2 * 2 * NS * P * (kK + 4) * sizeof(float) + 2 * 2 * NS * T * in_bytes + 2 * sizeof(uint64_t);
+  const size_t T = static_cast<size_t>(P) * kK, EPR = 128 / in_bytes;
+  const size_t rows = static_cast<size_t>(warps_per_cta_for(P)) * (32 / P);
+  const bool tma_shape = T % EPR == 0 && rows % 8 == 0;
+  const size_t stage = tma_shape ? 2 * 3 * rows * T * in_bytes : 0;
+  return 1024 + stage + 2 * 2 * NS * P * (kK + 4) * sizeof(float) + 2 * 2 * NS * T * in_bytes + 2 * sizeof(uint64_t);
 }
 
 // Lanes per channel: as few as keep enough warps in flight (each extra lane adds scan work), more

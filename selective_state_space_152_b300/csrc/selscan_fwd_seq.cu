@@ -370,23 +370,6 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   }
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// A 2-D map of a row-major [rows][inner] tensor with box [box_rows][box_inner] (inner fastest).
-template <typename Tin>
-bool encode_2d(EncodeTiled enc, CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-               uint32_t box_rows, CUtensorMapSwizzle swizzle) {
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner * sizeof(Tin)};
-  const cuuint32_t box[2] = {box_inner, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt = sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
 cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
   using C = SeqCfg<NS, Q, R, Tin>;

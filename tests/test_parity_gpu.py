@@ -20,13 +20,19 @@ pytestmark = pytest.mark.gpu
 
 # Both forward kernels: "seq" walks each row sequentially (rows spread over lanes), "chunk" splits
 # each row's sequence over lanes and joins them with a scan.  The library picks by shape; the tests
-# force each one through the SELSCAN_KERNEL override.
-KERNELS = ["seq", "chunk"]
+# force each one through the SELSCAN_KERNEL override.  "chunk_direct" is the chunked kernel with its
+# tensor-copy staging turned off (SELSCAN_STAGING=0), so that its direct-load path is also covered
+# on aligned inputs.
+KERNELS = ["seq", "chunk", "chunk_direct"]
 
 
 @pytest.fixture(params=KERNELS)
 def kernel(request, monkeypatch):
-    monkeypatch.setenv("SELSCAN_KERNEL", request.param)
+    monkeypatch.setenv("SELSCAN_KERNEL", "seq" if request.param == "seq" else "chunk")
+    if request.param == "chunk_direct":
+        monkeypatch.setenv("SELSCAN_STAGING", "0")
+    else:
+        monkeypatch.delenv("SELSCAN_STAGING", raising=False)
     return request.param
 
 
@@ -74,6 +80,34 @@ def test_small_shapes_full(case, kernel):
         inp["delta"] = si.f32_to_bf16_bits(d) if dt == "bf16" else d.astype(np.float32)
     ref, href = oracle.selscan_fwd(inp, delta_softplus=sp)
     got, hl = gpu_fwd(inp, delta_softplus=sp)
+    check_out(got, ref, dt)
+    check_h(hl, href)
+
+
+# Shapes for the chunked kernel's tensor-copy staging, forced onto 4, 8 and 16 lanes per channel
+# (channel blocks of 32, 16 and 8 rows; chunks of 64, 128 and 256 steps).  They cover ragged last
+# chunks, channel counts that leave part of the last block past `dim` (its rows read the next batch
+# entry's rows, or zeros past the tensor), dstate below the tile's 4/8/16 states, and both dtypes.
+STAGED = [
+    (31, 2, 40, 1000, 16, "bf16"),
+    (32, 3, 17, 264, 12, "bf16"),
+    (33, 1, 8, 4096, 16, "bf16"),
+    (34, 2, 24, 300, 5, "f32"),
+    (35, 1, 33, 772, 16, "f32"),
+    (36, 2, 16, 64, 3, "bf16"),
+]
+
+
+@pytest.mark.parametrize("lanes", ["4", "8", "16"])
+@pytest.mark.parametrize("case", STAGED, ids=[f"s{c[0]}_B{c[1]}D{c[2]}L{c[3]}N{c[4]}_{c[5]}" for c in STAGED])
+def test_chunked_staged_shapes(case, lanes, monkeypatch):
+    monkeypatch.setenv("SELSCAN_KERNEL", "chunk")
+    monkeypatch.setenv("SELSCAN_LANES", lanes)
+    monkeypatch.delenv("SELSCAN_STAGING", raising=False)
+    seed, Bsz, Dm, L, N, dt = case
+    inp = si.random_case(seed, Bsz, Dm, L, N, in_dtype=dt)
+    ref, href = oracle.selscan_fwd(inp)
+    got, hl = gpu_fwd(inp)
     check_out(got, ref, dt)
     check_h(hl, href)
 
