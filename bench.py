@@ -138,13 +138,19 @@ def max_over_ranks(seconds, dist, device):
     return float(tt.item())
 
 
-def kernel_source_hash():
+# The sources each kernel is built from (its own file and the shared device helpers).
+KERNEL_SOURCES = {"selscan_fwd": ("selscan_fwd.cu", "selscan_internal.cuh"),
+                  "selscan_step": ("selscan_step.cu", "selscan_internal.cuh")}
+
+
+def kernel_source_hash(kernel=None):
+    """Hash of a kernel's sources (all of csrc/ when kernel is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_152_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    names = KERNEL_SOURCES.get(kernel) or [n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh"))]
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -156,7 +162,7 @@ def recorded_traffic(kernel, workload, path=os.path.join(ROOT, "profiles", "ncu_
     except (OSError, ValueError):
         return None
     e = rec.get(kernel, {}).get(workload)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 

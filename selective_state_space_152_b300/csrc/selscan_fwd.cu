@@ -321,7 +321,9 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_WARPS_PER_SM / R)
   constexpr int T = C::T;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // The u, δ, z stage starts on a 1 KiB boundary (the period of the 128-byte swizzle).
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // (Offsetting the shared pointer itself keeps every derived pointer in the shared window, so the
+  // tile reads compile to shared loads rather than generic ones.)
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   unsigned char* stage = smem;                                                  // [2 buffers][3][SUBT][ROWS][128 B]
   float* tiles = reinterpret_cast<float*>(smem + C::kStageBytes);               // [2 buffers][2][NS][P][KP]
   Tin* raw = reinterpret_cast<Tin*>(smem + C::kStageBytes + C::kTileBytes);     // [2 buffers][RAW]
@@ -562,10 +564,10 @@ int pick_lanes(const FwdParams& p, int NS, size_t in_bytes) {
     if (smem_max <= 0) smem_max = 48 * 1024;
   }
   // Lane counts measured fastest on B300 for 16 states, by the number of (batch, channel) rows:
-  // 20480 rows -> 8 lanes, 12288 -> 4, 1536 -> 32.  Fewer lanes mean less scan work per step but
+  // 20480 and 12288 rows -> 4 lanes, 1536 -> 16.  Fewer lanes mean less scan work per step but
   // fewer warps; the thresholds sit between the measured shapes.
   const int64_t rows = p.batch * p.dim;
-  int P = rows >= 16384 ? 8 : rows >= 4096 ? 4 : rows >= 2048 ? 16 : 32;
+  int P = rows >= 4096 ? 4 : rows >= 512 ? 16 : 32;
   (void)sms;
   // SELSCAN_LANES (2, 4, 8, 16 or 32) overrides the choice; for tuning runs only.
   if (const char* e = getenv("SELSCAN_LANES")) {

@@ -67,7 +67,7 @@ def test_measured_peaks_fallback(tmp_path):
 
 def test_recorded_traffic_needs_the_current_sources(tmp_path):
     p = tmp_path / "traffic.json"
-    rec = {"selscan_fwd": {"w": {"source_hash": bench.kernel_source_hash(), "dram_bytes_per_launch": 123.0}},
+    rec = {"selscan_fwd": {"w": {"source_hash": bench.kernel_source_hash("selscan_fwd"), "dram_bytes_per_launch": 123.0}},
            "selscan_step": {"w": {"source_hash": "stale", "dram_bytes_per_launch": 5.0}}}
     p.write_text(json.dumps(rec))
     assert bench.recorded_traffic("selscan_fwd", "w", str(p)) == 123.0
