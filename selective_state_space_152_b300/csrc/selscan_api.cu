@@ -196,6 +196,10 @@ selscan_status_t selscan_fwd(const selscan_shape_t* shape, const void* u, const 
   p.vec_bc = aligned(B, 16) && aligned(C, 16) && L % vin == 0;
   p.vec_stage = p.vec_bc && p.vec_in;  // u, delta, z rows may be bulk-copied too
   p.use_tma = 0;
+  p.tblock = L;
+  p.nblocks = 1;
+  p.summ = nullptr;
+  p.start = nullptr;
   cudaError_t e = selscan::launch_fwd(p, shape->in_dtype, shape->out_dtype, s);
   return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
 }

@@ -601,16 +601,15 @@ cudaError_t dispatch_ns(const FwdParams& p, cudaStream_t s) {
 
 }  // namespace
 
-// The sequential kernel when there are enough rows to fill the GPU without splitting a row's sequence
-// (at least 32 rows per SM); otherwise the chunked scan.  SELSCAN_KERNEL=seq|chunk overrides the choice
-// (for tuning runs only).
+// The chunked scan when the rows alone give enough lanes (4 lanes per row); otherwise the sequential
+// kernel, which cuts the sequence into time blocks joined by a summary and a carry pass.
+// SELSCAN_KERNEL=seq|chunk overrides the choice (for tuning runs and tests).
 bool use_sequential(const FwdParams& p) {
   if (const char* e = getenv("SELSCAN_KERNEL")) {
     if (e[0] == 's') return true;
     if (e[0] == 'c') return false;
   }
-  (void)p;
-  return false;  // measured slower than the chunked scan on every workload tried so far
+  return p.batch * p.dim < 4096;
 }
 
 cudaError_t launch_fwd(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s) {

@@ -20,6 +20,7 @@
 // and one lane's states are one 128-bit shared load that every lane of a quarter-warp reads at the
 // same address (a broadcast).  The u, δ, z rows are stored with a 16-byte pad per row so that the
 // rows read by one quarter-warp fall in different bank groups.
+#include <cstdlib>
 #include <cstring>
 
 #include "selscan_internal.cuh"
@@ -108,6 +109,24 @@ __device__ __forceinline__ void store8(T* __restrict__ row, int64_t t, int64_t L
   }
 }
 
+// 4 consecutive outputs [t, t+4) of a row (one 16-byte store for fp32, 8-byte for bf16).
+template <typename T>
+__device__ __forceinline__ void store4(T* __restrict__ row, int64_t t, int64_t L, bool vec, const float (&y)[4]) {
+  if (vec && t + 4 <= L) {
+    if (sizeof(T) == 4) {
+      *reinterpret_cast<uint4*>(row + t) =
+          make_uint4(out_bits(y[0], T()), out_bits(y[1], T()), out_bits(y[2], T()), out_bits(y[3], T()));
+    } else {
+      *reinterpret_cast<uint2*>(row + t) = make_uint2(out_bits(y[0], T()) | (out_bits(y[1], T()) << 16),
+                                                      out_bits(y[2], T()) | (out_bits(y[3], T()) << 16));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+      if (t + i < L) row[t + i] = from_f32<T>(y[i]);
+  }
+}
+
 // 8 consecutive staged inputs [t, t+8) of CTA row r from a tensor's stage [SUBT][ROWS][EPR], written
 // by a 2-D tensor copy with the 128-byte swizzle: 16-byte chunk c of stage row r sits at chunk
 // position c ^ (r mod 8).  Steps past the end of the sequence were zero-filled by the copy.
@@ -124,11 +143,11 @@ __device__ __forceinline__ void stage8(Vec8<T>& s, const unsigned char* __restri
 
 // Transpose raw chunk rows [2][NS][T] (Tin) into the tile [2][T][TS] (fp32), zeroing states >= N and
 // steps >= L.  Work unit: one tensor, 4 states, 4 steps (steps fastest across threads).
-template <int NS, int Q, int R, typename Tin, bool MASK>
+template <int NS, int Q, int R, typename Tin, bool MASK, int NT = 2>
 __device__ __forceinline__ void transpose_chunk(const Tin* __restrict__ rb, float* __restrict__ tb, int tid,
                                                 int64_t t0, int64_t L, int N) {
   using C = SeqCfg<NS, Q, R, Tin>;
-  constexpr int T4 = C::T / 4, N4 = NS / 4, UNITS = 2 * N4 * T4;
+  constexpr int T4 = C::T / 4, N4 = NS / 4, UNITS = NT * N4 * T4;  // NT = 1: B only
   for (int unit = tid; unit < UNITS; unit += R * 32) {
     const int t4 = unit % T4, rest = unit / T4;
     const int n4 = rest % N4, tt = rest / N4;
@@ -166,14 +185,18 @@ __device__ __forceinline__ void transpose_chunk(const Tin* __restrict__ rb, floa
 #define SELSCAN_SEQ_WARPS_PER_SM 12
 #endif
 
-template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
+// SUMMARY: the summary pass of a time-blocked run (no C, y, z or out; writes the block's
+// zero-start end state and ΣΔ).  Otherwise the scan: time block blockIdx.z of the sequence, from h0
+// (block 0) or from its start state.
+template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS, bool SUMMARY>
 __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
     selscan_fwd_seq_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
   using C = SeqCfg<NS, Q, R, Tin>;
   constexpr int T = C::T, SB = C::SB, TS = C::TS, SPL = C::SPL, PAIRS = C::PAIRS, RPW = C::RPW;
   extern __shared__ __align__(128) unsigned char smem_dyn[];
-  unsigned char* smem_base = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  // (Offsetting the shared pointer itself keeps every derived pointer in the shared window, so the
+  // tile reads compile to shared loads rather than generic ones.)
+  unsigned char* smem_base = smem_dyn + ((1024u - (smem_addr(smem_dyn) & 1023u)) & 1023u);
   unsigned char* udz = smem_base;                                           // [2 buffers][3][SUBT][ROWS][EPR]
   Tin* raw = reinterpret_cast<Tin*>(smem_base + C::kUdzBytes);              // [2 buffers][2][NS][T]
   float* tiles = reinterpret_cast<float*>(smem_base + C::kUdzBytes + C::kRawBytes);  // [2 buffers][2][T][TS]
@@ -189,7 +212,13 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   const bool row_ok = d < p.dim;
   const int N = FULLN ? NS : p.dstate;
   const int64_t L = p.seqlen;
-  const int64_t nchunks = (L + T - 1) / T;
+  const int kblk = blockIdx.z;  // time block: steps [tbeg, tend)
+  const int64_t tbeg = static_cast<int64_t>(kblk) * p.tblock;
+  const int64_t tend = (tbeg + p.tblock) < L ? (tbeg + p.tblock) : L;
+  const int64_t c_begin = tbeg / T;               // tblock is a multiple of T
+  const int64_t nchunks = (tend - tbeg + T - 1) / T;
+  const int64_t grow = b * p.dim + d;             // global row of this lane
+  const int64_t rows_total = p.batch * p.dim;
   const Tin* __restrict__ Bsrc = static_cast<const Tin*>(p.B) + b * N * L;
   const Tin* __restrict__ Csrc = static_cast<const Tin*>(p.C) + b * N * L;
   const bool tma = p.use_tma;
@@ -198,16 +227,17 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   // batch entry b, and the CTA's rows of u, δ, z.  Parts of a box past the end of a tensor are
   // zero-filled and still count towards the expected bytes.
   const int row0 = static_cast<int>(b * p.dim + static_cast<int64_t>(blockIdx.x) * C::ROWS);
-  const int ntens = p.z ? 3 : 2;
-  auto issue = [&](int64_t c) {
-    const int t0 = static_cast<int>(c * T);
-    uint64_t* bar = &bars[c & 1];
+  const int ntens = SUMMARY ? 2 : (p.z ? 3 : 2);  // u, δ (, z)
+  // ci: chunk index within the time block (selects the buffer and the barrier phase).
+  auto issue = [&](int64_t ci) {
+    const int t0 = static_cast<int>((c_begin + ci) * T);
+    uint64_t* bar = &bars[ci & 1];
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(bar, static_cast<uint32_t>((2 * NS + ntens * C::ROWS) * T * sizeof(Tin)));
-    Tin* dst = raw + (c & 1) * C::RAW;
+    mbar_expect_tx(bar, static_cast<uint32_t>(((SUMMARY ? 1 : 2) * NS + ntens * C::ROWS) * T * sizeof(Tin)));
+    Tin* dst = raw + (ci & 1) * C::RAW;
     tma_load_2d(dst, &maps.B, t0, static_cast<int>(b * N), bar);
-    tma_load_2d(dst + NS * T, &maps.C, t0, static_cast<int>(b * N), bar);
-    unsigned char* st = udz + (c & 1) * (C::UDZ * sizeof(Tin));
+    if (!SUMMARY) tma_load_2d(dst + NS * T, &maps.C, t0, static_cast<int>(b * N), bar);
+    unsigned char* st = udz + (ci & 1) * (C::UDZ * sizeof(Tin));
     const CUtensorMap* m[3] = {&maps.u, &maps.delta, &maps.z};
     for (int k = 0; k < ntens; k++)
       for (int sub = 0; sub < C::SUBT; sub++)
@@ -236,7 +266,12 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
       const int n = n0 + 2 * i + k;
       const bool ok = row_ok && n < N;
       a[k] = ok ? p.A[d * N + n] * kLog2e : 0.f;
-      hh[k] = (ok && p.h0) ? p.h0[(b * p.dim + d) * N + n] : 0.f;
+      if (SUMMARY)
+        hh[k] = 0.f;
+      else if (kblk > 0)
+        hh[k] = ok ? p.start[(kblk * rows_total + grow) * N + n] : 0.f;
+      else
+        hh[k] = (ok && p.h0) ? p.h0[grow * N + n] : 0.f;
     }
     A2[i] = f2(a[0], a[1]);
     h[i] = f2(hh[0], hh[1]);
@@ -252,9 +287,10 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   Tout* __restrict__ o_row = static_cast<Tout*>(p.out) + row_off;
   const bool vec = p.vec_in && p.vec_out;
 
-  int64_t c = 0;
+  float S = 0.f;  // Σ Δ over the block (summary pass)
+  int64_t c = 0;  // chunk index within the time block
   for (; c < nchunks; c++) {
-    const int64_t t0 = c * T;
+    const int64_t t0 = (c_begin + c) * T;
     const Tin* rb = raw + (c & 1) * C::RAW;
     float* tb = tiles + (c & 1) * C::TILE;
     const bool tail = t0 + T > L;
@@ -271,9 +307,9 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
       __syncthreads();
     }
     if (FULLN && !tail)
-      transpose_chunk<NS, Q, R, Tin, false>(rb, tb, tid, t0, L, N);
+      transpose_chunk<NS, Q, R, Tin, false, SUMMARY ? 1 : 2>(rb, tb, tid, t0, L, N);
     else
-      transpose_chunk<NS, Q, R, Tin, true>(rb, tb, tid, t0, L, N);
+      transpose_chunk<NS, Q, R, Tin, true, SUMMARY ? 1 : 2>(rb, tb, tid, t0, L, N);
     __syncthreads();  // tile c complete; every warp has finished chunk c-1
     if (s_abort) break;
     if (tma && tid == 0 && c + 1 < nchunks) issue(c + 1);
@@ -292,8 +328,10 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
       if (ts >= L) break;
       const bool full = !tail || ts + SB <= L;
       float dl[SB], du[SB], y[SB];
+      Vec8<Tin> us_keep;  // this sub-block's u (the D skip is added after the state loop)
       {
-        Vec8<Tin> us, ds;
+        Vec8<Tin>& us = us_keep;
+        Vec8<Tin> ds;
         if (tma) {
           stage8<Tin, C::ROWS>(us, su, r_cta, sb);
           stage8<Tin, C::ROWS>(ds, sd, r_cta, sb);
@@ -301,17 +339,60 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
           load8<Tin>(us, u_row, ts, L, vec && full);
           load8<Tin>(ds, dl_row, ts, L, vec && full);
         }
-        // Straight-line over the 8 steps (no branches), so their exponential/log chains overlap.
+        if constexpr (Q == 2) {
+          // The row's two lanes each compute Δ for one half of the 8 steps (lane q: steps
+          // [4q, 4q + 4)) and swap halves with a shuffle, so no softplus is computed twice.
+          constexpr int HB = SB / 2;
+          float mine[HB], other[HB];
+#pragma unroll
+          for (int m = 0; m < HB; m++) {
+            const float x = (q ? ds.get(HB + m) : ds.get(m)) + bias;
+            const float delta = SOFTPLUS ? softplus_fast(x) : x;
+            mine[m] = (full || ts + q * HB + m < L) ? delta : 0.f;  // identity steps past the end
+            if (SUMMARY) S += mine[m];
+          }
+#pragma unroll
+          for (int m = 0; m < HB; m++) other[m] = __shfl_xor_sync(kFull, mine[m], RPW);
+#pragma unroll
+          for (int i = 0; i < SB; i++) {
+            const int m = i % HB;
+            dl[i] = ((i < HB) == (q == 0)) ? mine[m] : other[m];
+            du[i] = dl[i] * us.get(i);
+          }
+        } else {
+          // Straight-line over the 8 steps (no branches), so their exponential/log chains overlap.
+#pragma unroll
+          for (int i = 0; i < SB; i++) {
+            const float x = ds.get(i) + bias;
+            float delta = SOFTPLUS ? softplus_fast(x) : x;
+            delta = (full || ts + i < L) ? delta : 0.f;  // identity steps past the end
+            const float uu = us.get(i);
+            dl[i] = delta;
+            du[i] = delta * uu;
+            y[i] = Dd * uu;
+            if (SUMMARY) S += delta;
+          }
+        }
+      }
+      if (SUMMARY) {
+        // The block's end state from a zero start: the state recurrence only.
 #pragma unroll
         for (int i = 0; i < SB; i++) {
-          const float x = ds.get(i) + bias;
-          float delta = SOFTPLUS ? softplus_fast(x) : x;
-          delta = (full || ts + i < L) ? delta : 0.f;  // identity steps past the end
-          const float uu = us.get(i);
-          dl[i] = delta;
-          du[i] = delta * uu;
-          y[i] = Dd * uu;
+          const float2 dd = f2(dl[i], dl[i]), uu = f2(du[i], du[i]);
+          const float4* bq = reinterpret_cast<const float4*>(tB + (sb + i) * TS);
+#pragma unroll
+          for (int g = 0; g < SPL / 4; g++) {
+            const float4 bb = bq[g];
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+              const int pi = 2 * g + k;
+              const float2 e = mul2s(dd, A2[pi]);
+              const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
+              h[pi] = fma2s(ab, h[pi], mul2s(uu, k ? f2(bb.z, bb.w) : f2(bb.x, bb.y)));
+            }
+          }
         }
+        continue;
       }
       float part[SB];
 #pragma unroll
@@ -334,21 +415,44 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
         }
         part[i] = yp.x + yp.y;
       }
-      // The row's Q lanes each hold the sum over their states: add them up (8 independent shuffles).
+      if constexpr (Q == 2) {
+        // Reduce-scatter of the two lanes' partial sums: lane q keeps steps [4q, 4q + 4), adds the
+        // D skip, gates and stores them (4 shuffles instead of 8, and no silu computed twice).
+        constexpr int HB = SB / 2;
+        float yq[HB];
 #pragma unroll
-      for (int o = RPW; o < 32; o <<= 1)
+        for (int m = 0; m < HB; m++) {
+          const float send = q ? part[m] : part[HB + m];
+          const float keep = q ? part[HB + m] : part[m];
+          yq[m] = keep + __shfl_xor_sync(kFull, send, RPW);
+          const float uu = q ? us_keep.get(HB + m) : us_keep.get(m);
+          yq[m] = fmaf(Dd, uu, yq[m]);
+        }
+        if (z_row) {
+          Vec8<Tin> zs;
+          if (tma) stage8<Tin, C::ROWS>(zs, sz, r_cta, sb);
+          else load8<Tin>(zs, z_row, ts, L, vec && full);
 #pragma unroll
-        for (int i = 0; i < SB; i++) part[i] += __shfl_xor_sync(kFull, part[i], o);
+          for (int m = 0; m < HB; m++) yq[m] *= silu_fast(q ? zs.get(HB + m) : zs.get(m));
+        }
+        if (row_ok) store4<Tout>(o_row, ts + q * HB, L, vec && full, yq);
+      } else {
+        // The row's Q lanes each hold the sum over their states: add them up (8 independent shuffles).
 #pragma unroll
-      for (int i = 0; i < SB; i++) y[i] += part[i];
-      if (z_row) {
-        Vec8<Tin> zs;
-        if (tma) stage8<Tin, C::ROWS>(zs, sz, r_cta, sb);
-        else load8<Tin>(zs, z_row, ts, L, vec && full);
+        for (int o = RPW; o < 32; o <<= 1)
 #pragma unroll
-        for (int i = 0; i < SB; i++) y[i] *= silu_fast(zs.get(i));
+          for (int i = 0; i < SB; i++) part[i] += __shfl_xor_sync(kFull, part[i], o);
+#pragma unroll
+        for (int i = 0; i < SB; i++) y[i] += part[i];
+        if (z_row) {
+          Vec8<Tin> zs;
+          if (tma) stage8<Tin, C::ROWS>(zs, sz, r_cta, sb);
+          else load8<Tin>(zs, z_row, ts, L, vec && full);
+#pragma unroll
+          for (int i = 0; i < SB; i++) y[i] *= silu_fast(zs.get(i));
+        }
+        if (row_ok && q == 0) store8<Tout>(o_row, ts, L, vec && full, y);
       }
-      if (row_ok && q == 0) store8<Tout>(o_row, ts, L, vec && full, y);
     }
   }
 
@@ -359,7 +463,22 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
     }
     return;
   }
-  if (row_ok && p.h_last) {
+  if (SUMMARY) {
+    if constexpr (Q == 2) S += __shfl_xor_sync(kFull, S, RPW);  // each lane summed one half of the steps
+    if (row_ok) {
+      float* o = p.summ + (kblk * rows_total + grow) * (N + 1);
+#pragma unroll
+      for (int i = 0; i < PAIRS; i++)
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+          const int n = n0 + 2 * i + k;
+          if (n < N) o[n] = k ? h[i].y : h[i].x;
+        }
+      if (q == 0) o[N] = S;
+    }
+    return;
+  }
+  if (row_ok && p.h_last && kblk == p.nblocks - 1) {
 #pragma unroll
     for (int i = 0; i < PAIRS; i++)
 #pragma unroll
@@ -368,6 +487,41 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
         if (n < N) p.h_last[(b * p.dim + d) * N + n] = k ? h[i].y : h[i].x;
       }
   }
+}
+
+// Start state of every time block from the blocks' summaries: for each (row, state), in block order,
+// s ← 2^(A·log2e·ΣΔ) s + (zero-start end state of the block).  Block 0 starts from h0.
+__global__ void __launch_bounds__(256) selscan_carry_kernel(const FwdParams p) {
+  const int64_t rows = p.batch * p.dim;
+  const int N = p.dstate;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= rows * N) return;
+  const int64_t grow = idx / N;
+  const int n = static_cast<int>(idx - grow * N);
+  const int64_t d = grow % p.dim;
+  const float A2 = p.A[d * N + n] * kLog2e;
+  float st = p.h0 ? p.h0[grow * N + n] : 0.f;
+#pragma unroll 8
+  for (int k = 0; k < p.nblocks - 1; k++) {
+    const float* sm = p.summ + (k * rows + grow) * (N + 1);
+    st = fmaf(ex2_approx(A2 * sm[N]), st, sm[n]);
+    p.start[((k + 1) * rows + grow) * N + n] = st;
+  }
+}
+
+// Time blocks for a problem whose rows alone do not fill the GPU: enough blocks that the scan's CTAs
+// (row blocks x time blocks) fill the resident slots once, each block at least kMinTblock steps.
+// SELSCAN_TBLOCKS=n forces n blocks (for tuning runs and tests).
+constexpr int64_t kMinTblock = 512;
+int64_t choose_tblock(const FwdParams& p, int64_t row_blocks, int slots) {
+  const int64_t L = p.seqlen;
+  int64_t nb = row_blocks >= slots ? 1 : slots / (row_blocks > 0 ? row_blocks : 1);
+  if (const char* e = getenv("SELSCAN_TBLOCKS")) nb = atoi(e) > 0 ? atoi(e) : nb;
+  if (nb <= 1) return L;
+  int64_t tb = (L + nb - 1) / nb;
+  tb = (tb + 63) / 64 * 64;  // whole chunks
+  if (tb < kMinTblock) tb = kMinTblock;
+  return tb;
 }
 
 template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
@@ -389,12 +543,49 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
               encode_2d<Tin>(enc, &maps.C, p.C, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE);
     p.use_tma = ok;
   }
-  auto kern = selscan_fwd_seq_kernel<NS, Q, R, Tin, Tout, FULLN, SOFTPLUS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+  auto scan = selscan_fwd_seq_kernel<NS, Q, R, Tin, Tout, FULLN, SOFTPLUS, false>;
+  auto summary = selscan_fwd_seq_kernel<NS, Q, R, Tin, float, FULLN, SOFTPLUS, true>;
+  cudaError_t e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(summary, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((p.dim + C::ROWS - 1) / C::ROWS), static_cast<unsigned>(p.batch));
-  kern<<<grid, R * 32, C::kSmem, s>>>(p, maps);
-  return cudaGetLastError();
+  const int64_t row_blocks = ((p.dim + C::ROWS - 1) / C::ROWS) * p.batch;
+  int per_sm = 0, sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scan, R * 32, C::kSmem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  p.tblock = choose_tblock(p, row_blocks, sms * per_sm);
+  p.nblocks = static_cast<int>((p.seqlen + p.tblock - 1) / p.tblock);
+  const dim3 grid(static_cast<unsigned>((p.dim + C::ROWS - 1) / C::ROWS), static_cast<unsigned>(p.batch),
+                  static_cast<unsigned>(p.nblocks));
+  if (p.nblocks == 1) {
+    scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+    return cudaGetLastError();
+  }
+  // Stream-ordered scratch for the block summaries and start states, released on the same stream.
+  const int64_t N = p.dstate;
+  const size_t summ_floats = static_cast<size_t>(p.nblocks - 1) * rows * (N + 1);
+  const size_t start_floats = static_cast<size_t>(p.nblocks) * rows * N;
+  void* ws = nullptr;
+  e = cudaMallocAsync(&ws, (summ_floats + start_floats) * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  p.summ = static_cast<float*>(ws);
+  p.start = p.summ + summ_floats;
+  const dim3 sgrid(grid.x, grid.y, grid.z - 1);
+  summary<<<sgrid, R * 32, C::kSmem, s>>>(p, maps);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    const int64_t threads = static_cast<int64_t>(rows) * N;
+    selscan_carry_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(p);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+    e = cudaGetLastError();
+  }
+  const cudaError_t ef = cudaFreeAsync(ws, s);
+  return e != cudaSuccess ? e : ef;
 }
 
 #ifndef SELSCAN_SEQ_R

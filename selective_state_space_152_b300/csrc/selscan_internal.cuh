@@ -31,6 +31,15 @@ struct FwdParams {
   int vec_bc;   // B, C rows may be read with 16-byte vectors (and bulk-copied)
   int vec_stage;  // B, C and u, delta, z rows may all be bulk-copied
   int use_tma;    // set by a launcher: its kernel stages inputs with tensor copies
+  // Time blocks of the sequential kernel (nblocks = 1: one pass over the whole sequence).  With
+  // nblocks > 1 the sequence is cut into blocks of tblock steps (a multiple of 64): a summary pass
+  // writes each block's zero-start end state and ΣΔ to `summ` ([nblocks-1][rows][N+1]), a carry pass
+  // turns them into the start state of every block (`start`, [nblocks][rows][N]; block 0 starts
+  // from h0), and the scan pass runs every block from its start state.
+  int64_t tblock;
+  int nblocks;
+  float* summ;
+  float* start;
 };
 
 // Arguments of one selscan_step launch.

@@ -112,6 +112,34 @@ def test_chunked_staged_shapes(case, lanes, monkeypatch):
     check_h(hl, href)
 
 
+# Time blocks of the sequential kernel: the sequence is cut into blocks joined by a summary pass
+# (each block's zero-start end state and ΣΔ) and a carry pass.  Forced block counts on ragged
+# lengths, with and without h0, softplus on and off, fp32 and bf16.
+TBLOCKED = [
+    (41, 2, 5, 1500, 16, "bf16", True, True),
+    (42, 1, 3, 2049, 4, "f32", True, False),
+    (43, 3, 4, 1100, 12, "f32", False, True),
+    (44, 1, 40, 4096, 16, "bf16", True, True),
+]
+
+
+@pytest.mark.parametrize("nblocks", ["2", "3", "7"])
+@pytest.mark.parametrize("case", TBLOCKED, ids=[f"s{c[0]}_B{c[1]}D{c[2]}L{c[3]}N{c[4]}_{c[5]}" for c in TBLOCKED])
+def test_time_blocked_sequential(case, nblocks, monkeypatch):
+    monkeypatch.setenv("SELSCAN_KERNEL", "seq")
+    monkeypatch.setenv("SELSCAN_TBLOCKS", nblocks)
+    seed, Bsz, Dm, L, N, dt, hh, sp = case
+    inp = si.random_case(seed, Bsz, Dm, L, N, in_dtype=dt, has_h0=hh)
+    if not sp:  # keep Δ = δ + bias positive without softplus
+        inp["delta_bias"] = None
+        d = np.abs(si.bf16_bits_to_f32(inp["delta"]) if dt == "bf16" else inp["delta"]) * 0.05
+        inp["delta"] = si.f32_to_bf16_bits(d) if dt == "bf16" else d.astype(np.float32)
+    ref, href = oracle.selscan_fwd(inp, delta_softplus=sp)
+    got, hl = gpu_fwd(inp, delta_softplus=sp)
+    check_out(got, ref, dt)
+    check_h(hl, href)
+
+
 @pytest.mark.parametrize("name", ["mamba130m_layer", "long_seq_65k", "width_2p8b"])
 def test_workload_sampled_rows(name):
     w = si.WORKLOADS[name]
