@@ -29,8 +29,11 @@
  * Conventions for every entry point:
  *  - All tensor arguments are DEVICE pointers (cudaMalloc'd, or pinned host
  *    memory mapped into the device address space) to contiguous row-major
- *    arrays, last index fastest.  The caller owns every buffer; the library
- *    allocates no device memory and keeps no state between calls.
+ *    arrays, last index fastest.  The caller owns every buffer.  The library
+ *    keeps no state between calls; selscan_fwd takes stream-ordered scratch
+ *    (cudaMallocAsync / cudaFreeAsync on `stream`) for the time blocks of
+ *    problems with few rows (see selscan_fwd_noalloc for a variant that
+ *    allocates nothing).
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream).  A return of SELSCAN_OK means the work was
  *    enqueued; faults during execution surface at the caller's next
@@ -70,7 +73,8 @@ typedef enum {
   SELSCAN_ERR_UNSUPPORTED = 4, /* dstate > SELSCAN_MAX_DSTATE or an unknown dtype */
   SELSCAN_ERR_CUDA = 5,        /* a CUDA call failed; see selscan_last_cuda_error() */
   SELSCAN_ERR_POINTER = 6,     /* a pointer is not device-accessible or its extent leaves its allocation */
-  SELSCAN_ERR_ALIAS = 7        /* an output overlaps an input (other than h_last == h0) */
+  SELSCAN_ERR_ALIAS = 7,       /* an output overlaps an input (other than h_last == h0) */
+  SELSCAN_ERR_SCRATCH = 8      /* selscan_fwd_noalloc only: the problem needs more scratch than its fixed buffer */
 } selscan_status_t;
 
 /* Problem sizes.  For selscan_step, seqlen must be 1. */
@@ -116,6 +120,33 @@ selscan_status_t selscan_step(const selscan_shape_t* shape, const void* u, const
                               const void* B, const void* C, const float* D, const void* z,
                               const float* delta_bias, int delta_softplus, float* state, void* out,
                               void* stream);
+
+/*
+ * Selective-scan forward that allocates no memory at all: same arguments, layouts, validation and
+ * result (within fp32 rounding) as selscan_fwd.  It is for callers that cannot call cudaMalloc or
+ * cudaMallocAsync while they run, for example code that owns a fixed memory budget or that runs
+ * inside a framework which forbids allocation during execution.  (selscan_fwd may take stream-ordered
+ * scratch from the CUDA memory pool for problems with few rows, see below.)  The pages describe no
+ * such entry point; it is an engineering addition.
+ *
+ * It always runs the sequential kernel.  For problems with few rows that kernel cuts the sequence
+ * into time blocks and keeps, per block, a summary and a start state of every row:
+ *   ((blocks - 1) * (N + 1) + blocks * N) * batch * dim floats.
+ * These live in one fixed device array of SELSCAN_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library,
+ * reserved on every GPU that loads the library until the process exits.  A problem that would need
+ * more returns SELSCAN_ERR_SCRATCH and enqueues nothing (the 1 x 1536 x 65536 x 16 case needs about
+ * 2.4 MiB).  No part of the array has to start at zero: each call writes every entry it reads first.
+ *
+ * The first call on a device looks up the array's device address (once per device, with that
+ * device current); make that first call before any stream capture.  Every call shares the one
+ * array: calls whose work overlaps on the GPU (other streams, other host threads) race on it and
+ * must be serialised by the caller.
+ */
+#define SELSCAN_NOALLOC_SCRATCH_BYTES (8u << 20)
+selscan_status_t selscan_fwd_noalloc(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                                     const void* B, const void* C, const float* D, const void* z,
+                                     const float* delta_bias, int delta_softplus, const float* h0, void* out,
+                                     float* h_last, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* selscan_status_string(selscan_status_t status);

@@ -19,9 +19,10 @@ LIB_PATH = os.path.join(_HERE, "libselscan.so")
 
 SELSCAN_F32, SELSCAN_BF16 = 0, 1
 STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SELSCAN_ERR_ALIGN",
-          4: "SELSCAN_ERR_UNSUPPORTED", 5: "SELSCAN_ERR_CUDA", 6: "SELSCAN_ERR_POINTER", 7: "SELSCAN_ERR_ALIAS"}
+          4: "SELSCAN_ERR_UNSUPPORTED", 5: "SELSCAN_ERR_CUDA", 6: "SELSCAN_ERR_POINTER", 7: "SELSCAN_ERR_ALIAS",
+          8: "SELSCAN_ERR_SCRATCH"}
 EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
-            "selscan_abi_version")
+            "selscan_abi_version", "selscan_fwd_noalloc")
 
 
 class SelscanError(RuntimeError):
@@ -54,6 +55,8 @@ def load_library(path: Optional[str] = None):
     shp = ctypes.POINTER(SelscanShape)
     lib.selscan_fwd.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
     lib.selscan_fwd.restype = i32
+    lib.selscan_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
+    lib.selscan_fwd_noalloc.restype = i32
     lib.selscan_step.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
     lib.selscan_step.restype = i32
     lib.selscan_status_string.argtypes = [i32]
@@ -168,6 +171,37 @@ def selscan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softpl
     return out, h_last
 
 
+def selscan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
+                        out=None, h_last=None, stream=None):
+    """Selective-scan forward that allocates no device memory inside the library.
+
+    For callers that must not allocate while they run.  ``out`` (and
+    ``h_last`` if wanted) must be given: this function allocates nothing,
+    not even through torch.  The time-block scratch lives in one fixed
+    buffer of the library (see ``include/selscan.h``); calls whose work
+    overlaps on the GPU race on it.  Raises ``SelscanError`` with status
+    ``SELSCAN_ERR_SCRATCH`` if the problem needs more than that buffer holds.
+    """
+    lib = load_library()
+    if out is None:
+        raise ValueError("selscan_fwd_noalloc allocates nothing: pass `out`")
+    if u.dim() != 3 or B.dim() != 3:
+        raise ValueError("u must be [B, D, L] and B must be [B, N, L]")
+    Bsz, Dm, L = u.shape
+    N = B.shape[1]
+    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias), ("h0", h0), ("h_last", h_last)):
+        _need_f32(name, t)
+    for name, t in (("delta", delta), ("z", z), ("B", B), ("C", C)):
+        if t is not None and t.dtype != u.dtype:
+            raise TypeError(f"{name} must have u's dtype {u.dtype}")
+    shape = SelscanShape(Bsz, Dm, L, N, _dtype_code(u.dtype), _dtype_code(out.dtype))
+    st = lib.selscan_fwd_noalloc(ctypes.byref(shape), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                 _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(out),
+                                 _ptr(h_last), _stream_handle(stream))
+    _check(st)
+    return out, h_last
+
+
 def selscan_step(u, delta, A, B, C, state, D=None, z=None, delta_bias=None, delta_softplus: bool = True,
                  out=None, stream=None, out_dtype=None):
     """One recurrent decode step, updating ``state`` [B, D, N] (float32) in place.
@@ -195,5 +229,5 @@ def selscan_step(u, delta, A, B, C, state, D=None, z=None, delta_bias=None, delt
     return out
 
 
-__all__ = ["selscan_fwd", "selscan_step", "selscan_status_string", "selscan_abi_version",
+__all__ = ["selscan_fwd", "selscan_fwd_noalloc", "selscan_step", "selscan_status_string", "selscan_abi_version",
            "selscan_last_cuda_error", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED"]

@@ -22,6 +22,7 @@
 // rows read by one quarter-warp fall in different bank groups.
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "selscan_internal.cuh"
 
@@ -614,6 +615,137 @@ cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan
   }
   return out_dtype == SELSCAN_F32 ? dispatch_seq<__nv_bfloat16, float>(p, s)
                                   : dispatch_seq<__nv_bfloat16, __nv_bfloat16>(p, s);
+}
+
+// ---- selscan_fwd_noalloc: the time-block scratch in a fixed device array ---------------------------
+//
+// For callers that may not allocate memory while they run.  The summaries and start states of the
+// time blocks live in this array instead of stream-ordered scratch; it is reserved on every GPU that
+// loads the library, for the life of the process.  Host code may not use the array's name as a
+// device address (in host code it names a host-side stand-in), so its device address is looked up
+// once per device with cudaGetSymbolAddress, with that device current, and passed to the kernels.
+// Calls share the array: work of calls that overlaps on the GPU races on it.
+
+constexpr size_t kNoAllocFloats = SELSCAN_NOALLOC_SCRATCH_BYTES / sizeof(float);
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the array on the current device (looked up on the first call per device).
+cudaError_t noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+// As launch_seq_cfg, with the scratch taken from the fixed array.
+template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
+cudaError_t launch_seq_noalloc_cfg(const FwdParams& p_in, cudaStream_t s, bool* too_big) {
+  using C = SeqCfg<NS, Q, R, Tin>;
+  FwdParams p = p_in;
+  TmaMaps maps;
+  memset(&maps, 0, sizeof maps);
+  const EncodeTiled enc = reinterpret_cast<EncodeTiled>(tensor_map_encoder());
+  const uint64_t rows = static_cast<uint64_t>(p.batch * p.dim), bc_rows = static_cast<uint64_t>(p.batch * p.dstate);
+  p.use_tma = p.vec_stage && enc && rows < (1ull << 31) && p.seqlen < (1ll << 31);
+  if (p.use_tma) {
+    const uint64_t L = static_cast<uint64_t>(p.seqlen);
+    bool ok = encode_2d<Tin>(enc, &maps.u, p.u, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d<Tin>(enc, &maps.delta, p.delta, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              (!p.z || encode_2d<Tin>(enc, &maps.z, p.z, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+              encode_2d<Tin>(enc, &maps.B, p.B, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              encode_2d<Tin>(enc, &maps.C, p.C, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE);
+    p.use_tma = ok;
+  }
+  auto scan = selscan_fwd_seq_kernel<NS, Q, R, Tin, Tout, FULLN, SOFTPLUS, false>;
+  auto summary = selscan_fwd_seq_kernel<NS, Q, R, Tin, float, FULLN, SOFTPLUS, true>;
+  cudaError_t e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(summary, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+  if (e != cudaSuccess) return e;
+  const int64_t row_blocks = ((p.dim + C::ROWS - 1) / C::ROWS) * p.batch;
+  int per_sm = 0, sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scan, R * 32, C::kSmem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  p.tblock = choose_tblock(p, row_blocks, sms * per_sm);
+  p.nblocks = static_cast<int>((p.seqlen + p.tblock - 1) / p.tblock);
+  const dim3 grid(static_cast<unsigned>((p.dim + C::ROWS - 1) / C::ROWS), static_cast<unsigned>(p.batch),
+                  static_cast<unsigned>(p.nblocks));
+  if (p.nblocks == 1) {  // one pass: no scratch needed
+    scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+    return cudaGetLastError();
+  }
+  const int64_t N = p.dstate;
+  const size_t summ_floats = static_cast<size_t>(p.nblocks - 1) * rows * (N + 1);
+  const size_t start_floats = static_cast<size_t>(p.nblocks) * rows * N;
+  if (summ_floats + start_floats > kNoAllocFloats) {
+    *too_big = true;
+    return cudaSuccess;
+  }
+  float* ws = nullptr;
+  e = noalloc_scratch(&ws);
+  if (e != cudaSuccess) return e;
+  // Every summary entry is written by the summary pass and every start entry by the carry pass
+  // before it is read, so nothing in the array needs clearing.
+  p.summ = ws;
+  p.start = ws + summ_floats;
+  const dim3 sgrid(grid.x, grid.y, grid.z - 1);
+  summary<<<sgrid, R * 32, C::kSmem, s>>>(p, maps);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    const int64_t threads = static_cast<int64_t>(rows) * N;
+    selscan_carry_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(p);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+template <typename Tin, typename Tout, bool SOFTPLUS>
+cudaError_t dispatch_seq_noalloc_sp(const FwdParams& p, cudaStream_t s, bool* too_big) {
+  constexpr int R = SELSCAN_SEQ_R;
+  if (p.dstate == 16) return launch_seq_noalloc_cfg<16, 2, R, Tin, Tout, true, SOFTPLUS>(p, s, too_big);
+  if (p.dstate <= 4) return launch_seq_noalloc_cfg<4, 1, R, Tin, Tout, false, SOFTPLUS>(p, s, too_big);
+  if (p.dstate <= 8) return launch_seq_noalloc_cfg<8, 2, R, Tin, Tout, false, SOFTPLUS>(p, s, too_big);
+  return launch_seq_noalloc_cfg<16, 2, R, Tin, Tout, false, SOFTPLUS>(p, s, too_big);
+}
+
+template <typename Tin, typename Tout>
+cudaError_t dispatch_seq_noalloc(const FwdParams& p, cudaStream_t s, bool* too_big) {
+  return p.delta_softplus ? dispatch_seq_noalloc_sp<Tin, Tout, true>(p, s, too_big)
+                          : dispatch_seq_noalloc_sp<Tin, Tout, false>(p, s, too_big);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_seq_noalloc(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype,
+                                   cudaStream_t s, bool* too_big) {
+  *too_big = false;
+  if (in_dtype == SELSCAN_F32) {
+    return out_dtype == SELSCAN_F32 ? dispatch_seq_noalloc<float, float>(p, s, too_big)
+                                    : dispatch_seq_noalloc<float, __nv_bfloat16>(p, s, too_big);
+  }
+  return out_dtype == SELSCAN_F32 ? dispatch_seq_noalloc<__nv_bfloat16, float>(p, s, too_big)
+                                  : dispatch_seq_noalloc<__nv_bfloat16, __nv_bfloat16>(p, s, too_big);
 }
 
 cudaError_t read_seq_device_error(int* value, int reset) {

@@ -89,6 +89,10 @@ inline bool encode_2d(EncodeTiled enc, CUtensorMap* m, const void* base, uint64_
 cudaError_t launch_step(const StepParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
 // The sequential forward kernel (rows-parallel, no scan) used by launch_fwd for many-row problems.
 cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
+// The sequential kernel with its time-block scratch in the library's fixed device array (no
+// allocation).  Sets *too_big and enqueues nothing if the problem needs more than the array holds.
+cudaError_t launch_fwd_seq_noalloc(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype,
+                                   cudaStream_t s, bool* too_big);
 // Read (and optionally clear) the device-side failure words set by a kernel's bounded wait.
 cudaError_t read_device_error(int* value, int reset);
 cudaError_t read_seq_device_error(int* value, int reset);
