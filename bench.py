@@ -417,29 +417,33 @@ def run_decode(args, torch, ss, device, stream, flush, sms, hbm_gbs):
     state = t["h0"].clone()
     out = torch.empty((T, Bsz, Dm), device=device, dtype=torch.float32)
 
-    def run_all():
-        for s in range(T):
-            ss.selscan_step(t["u"][s], t["delta"][s], t["A"], t["B"][s], t["C"][s], state, D=t["D"], z=t["z"][s],
-                            delta_bias=t["delta_bias"], out=out[s], stream=stream)
+    def step(s):
+        ss.selscan_step(t["u"][s], t["delta"][s], t["A"], t["B"][s], t["C"][s], state, D=t["D"], z=t["z"][s],
+                        delta_bias=t["delta_bias"], out=out[s], stream=stream)
 
     for _ in range(2):
         state.copy_(t["h0"])
-        run_all()
+        for s in range(T):
+            step(s)
+    # Each step is timed on its own, after an L2 flush: the 84 MB state would otherwise stay partly
+    # in the 126 MB L2 from one step to the next, which a model with many layers does not see.
     reps = 5
-    times = []
-    for _ in range(reps):
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(reps * T)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(reps * T)]
+    for r in range(reps):
         state.copy_(t["h0"])
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        run_all()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1) / 1e3)
-    secs = statistics.median(times)
+        for s in range(T):
+            flush.zero_()
+            starts[r * T + s].record(stream)
+            step(s)
+            ends[r * T + s].record(stream)
+    torch.cuda.synchronize()
+    per_rep = [sum(starts[r * T + s].elapsed_time(ends[r * T + s]) for s in range(T)) / 1e3 for r in range(reps)]
+    secs = statistics.median(per_rep)
     wk = step_work(Bsz, Dm, N)
     gbs = wk["bytes"] * T / secs / 1e9
     return {"workload": "decode_step", "batch": Bsz, "dim": Dm, "dstate": N, "steps": T,
+            "l2": "flushed (256 MiB write) before every step, outside its events",
             "elems_per_s": Bsz * Dm * T / secs, "us_per_step": secs / T * 1e6,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs,
                          "traffic": recorded_traffic("selscan_step", "decode_step")},

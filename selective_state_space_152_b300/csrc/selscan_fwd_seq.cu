@@ -33,17 +33,26 @@ __device__ int g_selscan_seq_error = 0;
 
 namespace {
 
+// Steps per chunk (32 or 64).  32 halves the shared memory of a CTA, so that 16 warps fit on an SM
+// (measured faster on B300 for 1536 and 20480 rows of 16 states).
+#ifndef SELSCAN_SEQ_T
+#define SELSCAN_SEQ_T 32
+#endif
+
 template <int NS, int Q, int R, typename Tin>
 struct SeqCfg {
   static constexpr int SPL = NS / Q;  // states per lane
   static constexpr int PAIRS = SPL / 2;
   static constexpr int RPW = 32 / Q;    // rows per warp
   static constexpr int ROWS = R * RPW;  // rows per CTA
-  static constexpr int T = 64;          // steps per chunk
-  static constexpr int SB = 8;          // steps per sub-block
-  static constexpr int TS = NS + 4;     // floats per step in the tile (padded: transposing stores spread over banks)
-  static constexpr int EPR = 128 / static_cast<int>(sizeof(Tin));  // inputs per 128-byte swizzled stage row
+  static constexpr int T = SELSCAN_SEQ_T;  // steps per chunk
+  static constexpr int SB = 8;             // steps per sub-block
+  static constexpr int TS = NS + 4;        // floats per step in the tile (padded: transposing stores spread over banks)
+  // Stage rows of RB bytes (128, or 64 for 32 bf16 steps), written with the swizzle of that width.
+  static constexpr int RB = T * static_cast<int>(sizeof(Tin)) < 128 ? T * static_cast<int>(sizeof(Tin)) : 128;
+  static constexpr int EPR = RB / static_cast<int>(sizeof(Tin));  // inputs per stage row
   static constexpr int SUBT = T / EPR;                            // stage sub-tiles per tensor and chunk
+  static constexpr CUtensorMapSwizzle kSwizzle = RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   static constexpr int UDZ = 3 * T * ROWS;  // elements of one u, δ, z stage: [3][SUBT][ROWS][EPR]
   static constexpr int RAW = 2 * NS * T;    // raw elements of one chunk: B rows then C rows, [2][NS][T]
   static constexpr int TILE = 2 * T * TS;   // floats of one transposed tile: [2][T][TS]
@@ -54,7 +63,8 @@ struct SeqCfg {
   // every 8 rows of 128 bytes and is computed from the address).
   static constexpr size_t kSmem = 1024 + kUdzBytes + kRawBytes + kTileBytes + 2 * sizeof(uint64_t);
   static_assert(SPL >= 4 && SPL % 4 == 0, "each lane owns whole groups of 4 states");
-  static_assert((ROWS * 128) % 1024 == 0, "stage sub-tiles must keep 1 KiB alignment");
+  static_assert(RB == 128 || RB == 64, "stage rows of 64 or 128 bytes");
+  static_assert((ROWS * RB) % 1024 == 0, "stage sub-tiles must keep 1 KiB alignment");
 };
 
 // 8 consecutive inputs of a row as 16-byte vectors.
@@ -128,17 +138,19 @@ __device__ __forceinline__ void store4(T* __restrict__ row, int64_t t, int64_t L
   }
 }
 
-// 8 consecutive staged inputs [t, t+8) of CTA row r from a tensor's stage [SUBT][ROWS][EPR], written
-// by a 2-D tensor copy with the 128-byte swizzle: 16-byte chunk c of stage row r sits at chunk
-// position c ^ (r mod 8).  Steps past the end of the sequence were zero-filled by the copy.
-template <typename T, int ROWS>
+// 8 consecutive staged inputs [t, t+8) of CTA row r from a tensor's stage [SUBT][ROWS][RB bytes],
+// written by a 2-D tensor copy with the RB-byte swizzle: 16-byte chunk c of stage row r sits at chunk
+// position c ^ (r mod 8) for 128-byte rows, c ^ ((r / 2) mod 4) for 64-byte rows (each sub-tile starts
+// on a 1 KiB boundary).  Steps past the end of the sequence were zero-filled by the copy.
+template <typename T, int ROWS, int RB>
 __device__ __forceinline__ void stage8(Vec8<T>& s, const unsigned char* __restrict__ stage, int r, int t) {
-  constexpr int kPerVec = Vec8<T>::kPerVec, EPR = 128 / static_cast<int>(sizeof(T));
+  constexpr int kPerVec = Vec8<T>::kPerVec, EPR = RB / static_cast<int>(sizeof(T));
+  const int swz = RB == 128 ? (r & 7) : ((r >> 1) & 3);
 #pragma unroll
   for (int q = 0; q < Vec8<T>::kVecs; q++) {
     const int e = t + q * kPerVec;
     const int sub = e / EPR, chunk = (e % EPR) / kPerVec;
-    s.v[q] = *reinterpret_cast<const uint4*>(stage + (sub * ROWS + r) * 128 + ((chunk ^ (r & 7)) << 4));
+    s.v[q] = *reinterpret_cast<const uint4*>(stage + (sub * ROWS + r) * RB + ((chunk ^ swz) << 4));
   }
 }
 
@@ -183,7 +195,7 @@ __device__ __forceinline__ void transpose_chunk(const Tin* __restrict__ rb, floa
 }
 
 #ifndef SELSCAN_SEQ_WARPS_PER_SM
-#define SELSCAN_SEQ_WARPS_PER_SM 12
+#define SELSCAN_SEQ_WARPS_PER_SM 16
 #endif
 
 // SUMMARY: the summary pass of a time-blocked run (no C, y, z or out; writes the block's
@@ -242,7 +254,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
     const CUtensorMap* m[3] = {&maps.u, &maps.delta, &maps.z};
     for (int k = 0; k < ntens; k++)
       for (int sub = 0; sub < C::SUBT; sub++)
-        tma_load_2d(st + (k * C::SUBT + sub) * C::ROWS * 128, m[k], t0 + sub * C::EPR, row0, bar);
+        tma_load_2d(st + (k * C::SUBT + sub) * C::ROWS * C::RB, m[k], t0 + sub * C::EPR, row0, bar);
   };
 
   if (tid == 0) {
@@ -321,8 +333,8 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
     // rows: computed on, never stored).
     const int r_cta = (tid >> 5) * RPW + rw;
     const unsigned char* su = udz + (c & 1) * (C::UDZ * sizeof(Tin));
-    const unsigned char* sd = su + C::SUBT * C::ROWS * 128;
-    const unsigned char* sz = sd + C::SUBT * C::ROWS * 128;
+    const unsigned char* sd = su + C::SUBT * C::ROWS * C::RB;
+    const unsigned char* sz = sd + C::SUBT * C::ROWS * C::RB;
 #pragma unroll 1
     for (int sb = 0; sb < T; sb += SB) {
       const int64_t ts = t0 + sb;
@@ -334,8 +346,8 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
         Vec8<Tin>& us = us_keep;
         Vec8<Tin> ds;
         if (tma) {
-          stage8<Tin, C::ROWS>(us, su, r_cta, sb);
-          stage8<Tin, C::ROWS>(ds, sd, r_cta, sb);
+          stage8<Tin, C::ROWS, C::RB>(us, su, r_cta, sb);
+          stage8<Tin, C::ROWS, C::RB>(ds, sd, r_cta, sb);
         } else {
           load8<Tin>(us, u_row, ts, L, vec && full);
           load8<Tin>(ds, dl_row, ts, L, vec && full);
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
         }
         if (z_row) {
           Vec8<Tin> zs;
-          if (tma) stage8<Tin, C::ROWS>(zs, sz, r_cta, sb);
+          if (tma) stage8<Tin, C::ROWS, C::RB>(zs, sz, r_cta, sb);
           else load8<Tin>(zs, z_row, ts, L, vec && full);
 #pragma unroll
           for (int m = 0; m < HB; m++) yq[m] *= silu_fast(q ? zs.get(HB + m) : zs.get(m));
@@ -447,7 +459,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
         for (int i = 0; i < SB; i++) y[i] += part[i];
         if (z_row) {
           Vec8<Tin> zs;
-          if (tma) stage8<Tin, C::ROWS>(zs, sz, r_cta, sb);
+          if (tma) stage8<Tin, C::ROWS, C::RB>(zs, sz, r_cta, sb);
           else load8<Tin>(zs, z_row, ts, L, vec && full);
 #pragma unroll
           for (int i = 0; i < SB; i++) y[i] *= silu_fast(zs.get(i));
@@ -537,9 +549,9 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
   p.use_tma = p.vec_stage && enc && rows < (1ull << 31) && p.seqlen < (1ll << 31);
   if (p.use_tma) {
     const uint64_t L = static_cast<uint64_t>(p.seqlen);
-    bool ok = encode_2d<Tin>(enc, &maps.u, p.u, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d<Tin>(enc, &maps.delta, p.delta, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              (!p.z || encode_2d<Tin>(enc, &maps.z, p.z, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+    bool ok = encode_2d<Tin>(enc, &maps.u, p.u, L, rows, C::EPR, C::ROWS, C::kSwizzle) &&
+              encode_2d<Tin>(enc, &maps.delta, p.delta, L, rows, C::EPR, C::ROWS, C::kSwizzle) &&
+              (!p.z || encode_2d<Tin>(enc, &maps.z, p.z, L, rows, C::EPR, C::ROWS, C::kSwizzle)) &&
               encode_2d<Tin>(enc, &maps.B, p.B, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
               encode_2d<Tin>(enc, &maps.C, p.C, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE);
     p.use_tma = ok;
@@ -590,7 +602,7 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
 }
 
 #ifndef SELSCAN_SEQ_R
-#define SELSCAN_SEQ_R 2
+#define SELSCAN_SEQ_R 4
 #endif
 
 template <typename Tin, typename Tout, bool SOFTPLUS>
@@ -664,9 +676,9 @@ cudaError_t launch_seq_noalloc_cfg(const FwdParams& p_in, cudaStream_t s, bool* 
   p.use_tma = p.vec_stage && enc && rows < (1ull << 31) && p.seqlen < (1ll << 31);
   if (p.use_tma) {
     const uint64_t L = static_cast<uint64_t>(p.seqlen);
-    bool ok = encode_2d<Tin>(enc, &maps.u, p.u, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d<Tin>(enc, &maps.delta, p.delta, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              (!p.z || encode_2d<Tin>(enc, &maps.z, p.z, L, rows, C::EPR, C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+    bool ok = encode_2d<Tin>(enc, &maps.u, p.u, L, rows, C::EPR, C::ROWS, C::kSwizzle) &&
+              encode_2d<Tin>(enc, &maps.delta, p.delta, L, rows, C::EPR, C::ROWS, C::kSwizzle) &&
+              (!p.z || encode_2d<Tin>(enc, &maps.z, p.z, L, rows, C::EPR, C::ROWS, C::kSwizzle)) &&
               encode_2d<Tin>(enc, &maps.B, p.B, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
               encode_2d<Tin>(enc, &maps.C, p.C, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE);
     p.use_tma = ok;
