@@ -360,6 +360,8 @@ def run_ours(args, rank, world, local_rank, dist):
         result["e2e"] = run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world)
     if rank == 0 and world == 1 and not args.no_decode:
         result["decode"] = run_decode(args, torch, ss, device, stream, flush, sms, hbm_gbs)
+    if rank == 0 and world == 1 and not args.no_options:
+        result["options"] = run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, w, budget_cpu_s=args.cpu_budget)
     return result
@@ -405,6 +407,33 @@ def run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world):
     return {"value": Bsz * Dm * L * steps * world / secs, "unit": "elems/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": secs / steps * 1e3,
             "gpu_launches": steps}
+
+
+def run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz, steps=50):
+    """Secondary: selscan_fwd_ex on the same workload with each option (reverse scan; exact
+    zero-order-hold input matrix), each step timed after an L2 flush, against the same roofline."""
+    res = {}
+    for name, kw in (("reverse", dict(reverse=True)), ("zoh", dict(zoh=True))):
+        def call():
+            ss.selscan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                              delta_bias=t["delta_bias"], delta_softplus=True, h0=t["h0"], out=out, h_last=h_last,
+                              stream=stream, **kw)
+
+        for _ in range(3):
+            flush.zero_()
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        secs = sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3 / steps
+        roof = roofline_entry(work, secs, sms, hbm_gbs, sm_mhz)
+        res[name] = {"us_per_call": secs * 1e6, "elems_per_s": work["elements"] / secs,
+                     "roofline_frac": roof["frac"], "gpu_launches": steps}
+    return res
 
 
 def run_decode(args, torch, ss, device, stream, flush, sms, hbm_gbs):
@@ -519,6 +548,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-options", action="store_true", help="skip the reverse / zero-order-hold timings")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

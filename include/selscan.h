@@ -122,6 +122,31 @@ selscan_status_t selscan_step(const selscan_shape_t* shape, const void* u, const
                               void* stream);
 
 /*
+ * Selective-scan forward with options (flags, OR-ed):
+ *
+ *   SELSCAN_FLAG_REVERSE  scan from t = L-1 down to 0: h_t = Ā_t·h_{t+1} + B̄_t·u_t (h_L = h0),
+ *                         y_t = Σ_n C[b,n,t]·h_t[n] + D[d]·u_t; h_last is the state after t = 0.
+ *                         This is the backward direction of a bidirectional Mamba layer ("Mamba架构与
+ *                         SSM模型：高效序列建模技术解析" §3.2 names a bidirectional option; "Mamba:
+ *                         Linear-Time Sequence Modeling with Selective State Spaces" mentions
+ *                         bidirectional use for DNA).
+ *   SELSCAN_FLAG_ZOH      exact zero-order hold for the input matrix, B̄ = (exp(Δ·A) - 1)/A · B per
+ *                         state (diagonal A; Δ·B at A = 0), instead of B̄ = Δ·B
+ *                         ("Mamba架构与SSM模型：高效序列建模技术解析" §2.1 prints
+ *                         B̄ = (ΔA)^{-1}(exp(ΔA) - I)·ΔB).
+ *
+ * Arguments, layouts, checks and errors are those of selscan_fwd.  flags = 0 computes exactly what
+ * selscan_fwd computes.  Unknown flag bits return SELSCAN_ERR_UNSUPPORTED.  It always runs the
+ * sequential kernel (with time blocks and their stream-ordered scratch for problems with few rows).
+ */
+#define SELSCAN_FLAG_REVERSE 1u
+#define SELSCAN_FLAG_ZOH 2u
+selscan_status_t selscan_fwd_ex(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                                const void* B, const void* C, const float* D, const void* z,
+                                const float* delta_bias, int delta_softplus, const float* h0, void* out,
+                                float* h_last, unsigned flags, void* stream);
+
+/*
  * Selective-scan forward that allocates no memory at all: same arguments, layouts, validation and
  * result (within fp32 rounding) as selscan_fwd.  It is for callers that cannot call cudaMalloc or
  * cudaMallocAsync while they run, for example code that owns a fixed memory budget or that runs

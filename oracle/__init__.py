@@ -43,7 +43,8 @@ def build() -> str:
 
 def _bind(lib):
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-    lib.oracle_selscan_fwd.argtypes = [i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p, i32, p, p, i32, p, i64, p, p, i32]
+    lib.oracle_selscan_fwd.argtypes = [i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p, i32, p, p, i32, i32, p, i64, p, p,
+                                       i32]
     lib.oracle_selscan_fwd.restype = i32
     lib.oracle_selscan_step.argtypes = [i64, i64, i64, i32, p, p, p, p, p, p, p, p, i32, p, p]
     lib.oracle_selscan_step.restype = i32
@@ -85,7 +86,8 @@ def _f32(a):
 
 
 def selscan_fwd(inp: Dict[str, object], delta_softplus: bool = True, rows: Optional[Sequence[int]] = None,
-                reverse: bool = False, nthreads: Optional[int] = None, h0_f64: Optional[np.ndarray] = None, lib=None):
+                reverse: bool = False, nthreads: Optional[int] = None, h0_f64: Optional[np.ndarray] = None, lib=None,
+                zoh: bool = False):
     """Run the fp64 forward on an input dict (see ``seeded_inputs.make_inputs``).
 
     Returns ``(out, h_last)`` as float64 arrays shaped ``[B, D, L]`` and
@@ -113,7 +115,7 @@ def selscan_fwd(inp: Dict[str, object], delta_softplus: bool = True, rows: Optio
     rc = lib.oracle_selscan_fwd(Bsz, Dm, L, N, _DT[dt], _ptr(u), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm),
                                 _ptr(D), _ptr(z), _ptr(bias), int(bool(delta_softplus)), _ptr(h0),
                                 _ptr(None if h0_f64 is None else np.ascontiguousarray(h0_f64, dtype=np.float64)),
-                                int(bool(reverse)),
+                                int(bool(reverse)), int(bool(zoh)),
                                 rp, nr, _ptr(out), _ptr(hl), int(nth))
     if rc != 0:
         raise ValueError("oracle_selscan_fwd rejected its arguments")

@@ -31,8 +31,12 @@
  *    the next, which is what h0 / h_last expose.
  *
  * Readings where the pages leave a step open:
- *  - B̄ is taken as Δ·B (the simplified discretisation of the input matrix),
- *    not the exact ZOH form (ΔA)^{-1}(exp(ΔA)-I)·ΔB that §2.1 also prints.
+ *  - B̄ is taken as Δ·B (the simplified discretisation of the input matrix).
+ *    With `zoh` it is the exact zero-order-hold form (ΔA)^{-1}(exp(ΔA)-I)·ΔB
+ *    that "Mamba架构与SSM模型：高效序列建模技术解析" §2.1 prints; for the
+ *    diagonal A this is (exp(ΔA_n) - 1)/A_n · B_n per state, Δ·B_n at A_n = 0.
+ *  - `reverse` runs the same recurrence from t = L-1 down to 0 (the backward
+ *    direction of a bidirectional layer): h_t = Ā_t·h_{t+1} + B̄_t·u_t.
  *  - The gate multiplies the whole y, including the D·u term.
  *  - softplus is the exact log(1+e^x), evaluated as max(x,0) + log1p(e^{-|x|}).
  *  - silu(z) = z / (1 + e^{-z}).
@@ -76,6 +80,7 @@ typedef struct {
   const double* h0_f64; /* fp64 start state; takes precedence over h0 */
   int delta_softplus;
   int reverse; /* process t from L-1 down to 0 (bidirectional variant) */
+  int zoh;     /* exact zero-order-hold input matrix instead of Δ·B */
   /* rows to compute: flat indices b*dim + d; NULL = all rows */
   const int64_t* rows;
   int64_t nrows;
@@ -109,7 +114,10 @@ static void scan_row(const fwd_job* j, int64_t b, int64_t d, double* out_row, do
       const double Cv = load_in(j->C, bc, j->in_dtype);
       const double a = (double)j->A[d * N + n];
       const double abar = exp(dt * a);     /* Ā = exp(Δ·A) */
-      h[n] = abar * h[n] + dt * Bv * u;    /* h_t = Ā·h_{t-1} + Δ·B·u */
+      /* B̄ = Δ·B, or with zoh the exact zero-order hold (ΔA)^{-1}(exp(ΔA) - 1)·ΔB = (exp(ΔA) - 1)/A·B,
+       * whose limit at A = 0 is Δ·B. */
+      const double bbar = (j->zoh && a != 0.0) ? expm1(dt * a) / a : dt;
+      h[n] = abar * h[n] + bbar * Bv * u;  /* h_t = Ā·h_{t-1} + B̄·u */
       y += Cv * h[n];                      /* C·h_t reads the updated state */
     }
     y += Dd * u;
@@ -143,7 +151,8 @@ static void* fwd_worker(void* arg) {
 int oracle_selscan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype,
                        const void* u, const void* delta, const float* A, const void* B, const void* C,
                        const float* D, const void* z, const float* delta_bias, int delta_softplus,
-                       const float* h0, const double* h0_f64, int reverse, const int64_t* rows, int64_t nrows,
+                       const float* h0, const double* h0_f64, int reverse, int zoh, const int64_t* rows,
+                       int64_t nrows,
                        double* out,
                        double* h_last, int nthreads) {
   if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1 || dstate > 64) return -1;
@@ -168,6 +177,7 @@ int oracle_selscan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstat
   j.h0_f64 = h0_f64;
   j.delta_softplus = delta_softplus;
   j.reverse = reverse;
+  j.zoh = zoh;
   j.rows = rows;
   j.nrows = nrows;
   j.out = out;

@@ -22,7 +22,8 @@ STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SE
           4: "SELSCAN_ERR_UNSUPPORTED", 5: "SELSCAN_ERR_CUDA", 6: "SELSCAN_ERR_POINTER", 7: "SELSCAN_ERR_ALIAS",
           8: "SELSCAN_ERR_SCRATCH"}
 EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
-            "selscan_abi_version", "selscan_fwd_noalloc")
+            "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex")
+SELSCAN_FLAG_REVERSE, SELSCAN_FLAG_ZOH = 1, 2
 
 
 class SelscanError(RuntimeError):
@@ -55,6 +56,8 @@ def load_library(path: Optional[str] = None):
     shp = ctypes.POINTER(SelscanShape)
     lib.selscan_fwd.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
     lib.selscan_fwd.restype = i32
+    lib.selscan_fwd_ex.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, ctypes.c_uint, vp]
+    lib.selscan_fwd_ex.restype = i32
     lib.selscan_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
     lib.selscan_fwd_noalloc.restype = i32
     lib.selscan_step.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
@@ -171,6 +174,36 @@ def selscan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softpl
     return out, h_last
 
 
+def selscan_fwd_ex(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
+                   out=None, h_last=None, stream=None, out_dtype=None, return_h_last: bool = False,
+                   reverse: bool = False, zoh: bool = False):
+    """selscan_fwd with options: ``reverse`` scans from the last step to the first (h_last is the
+    state after step 0); ``zoh`` uses the exact zero-order-hold input matrix (exp(ΔA) - 1)/A·B
+    instead of Δ·B.  Arguments and return value as for ``selscan_fwd``."""
+    torch = _torch()
+    lib = load_library()
+    if u.dim() != 3 or B.dim() != 3:
+        raise ValueError("u must be [B, D, L] and B must be [B, N, L]")
+    Bsz, Dm, L = u.shape
+    N = B.shape[1]
+    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias), ("h0", h0), ("h_last", h_last)):
+        _need_f32(name, t)
+    for name, t in (("delta", delta), ("z", z), ("B", B), ("C", C)):
+        if t is not None and t.dtype != u.dtype:
+            raise TypeError(f"{name} must have u's dtype {u.dtype}")
+    if out is None:
+        out = torch.empty((Bsz, Dm, L), device=u.device, dtype=out_dtype or torch.float32)
+    if h_last is None and return_h_last:
+        h_last = torch.empty((Bsz, Dm, N), device=u.device, dtype=torch.float32)
+    flags = (SELSCAN_FLAG_REVERSE if reverse else 0) | (SELSCAN_FLAG_ZOH if zoh else 0)
+    shape = SelscanShape(Bsz, Dm, L, N, _dtype_code(u.dtype), _dtype_code(out.dtype))
+    st = lib.selscan_fwd_ex(ctypes.byref(shape), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                            _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(out), _ptr(h_last), flags,
+                            _stream_handle(stream))
+    _check(st)
+    return out, h_last
+
+
 def selscan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
                         out=None, h_last=None, stream=None):
     """Selective-scan forward that allocates no device memory inside the library.
@@ -229,5 +262,5 @@ def selscan_step(u, delta, A, B, C, state, D=None, z=None, delta_bias=None, delt
     return out
 
 
-__all__ = ["selscan_fwd", "selscan_fwd_noalloc", "selscan_step", "selscan_status_string", "selscan_abi_version",
+__all__ = ["selscan_fwd", "selscan_fwd_ex", "selscan_fwd_noalloc", "selscan_step", "selscan_status_string", "selscan_abi_version",
            "selscan_last_cuda_error", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED"]

@@ -198,10 +198,33 @@ __device__ __forceinline__ void transpose_chunk(const Tin* __restrict__ rb, floa
 #define SELSCAN_SEQ_WARPS_PER_SM 16
 #endif
 
+// The input-matrix factor of one state pair: Δ·u (the plain discretisation B̄ = Δ·B), or with ZOH the
+// exact zero-order hold B̄ = (exp(ΔA) - 1)/A · B ("Mamba架构与SSM模型：高效序列建模技术解析" §2.1, for
+// a diagonal A): u·(Ā - 1)/A where |ΔA| >= 1/16, and Δu·φ(ΔA) with the series
+// φ(x) = (e^x - 1)/x = 1 + x/2 + x²/6 + x³/24 + x⁴/120 below (truncation error < 1.3e-9 there, where
+// Ā - 1 would lose its leading digits).  At A = 0 the series gives Δu, the limit of the exact form.
+template <bool ZOH>
+__device__ __forceinline__ float2 input_factor(float2 du, float2 e, float2 ab, float2 inv_a, float uu) {
+  if (!ZOH) return du;
+  const float2 x = mul2s(e, f2(kLn2, kLn2));  // ΔA
+  float2 phi = fma2s(x, f2(1.f / 120.f, 1.f / 120.f), f2(1.f / 24.f, 1.f / 24.f));
+  phi = fma2s(x, phi, f2(1.f / 6.f, 1.f / 6.f));
+  phi = fma2s(x, phi, f2(0.5f, 0.5f));
+  phi = fma2s(x, phi, f2(1.f, 1.f));
+  const float2 small = mul2s(du, phi);
+  const float2 big = mul2s(add2s(ab, f2(-1.f, -1.f)), mul2s(inv_a, f2(uu, uu)));
+  return f2(fabsf(x.x) < 0.0625f ? small.x : big.x, fabsf(x.y) < 0.0625f ? small.y : big.y);
+}
+
 // SUMMARY: the summary pass of a time-blocked run (no C, y, z or out; writes the block's
 // zero-start end state and ΣΔ).  Otherwise the scan: time block blockIdx.z of the sequence, from h0
-// (block 0) or from its start state.
-template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS, bool SUMMARY>
+// (the first block in scan order) or from its start state.
+// REV: the scan runs from t = L-1 down to 0 (the reverse direction of a bidirectional layer): chunks,
+// sub-blocks and steps are taken in reverse order and h_last is the state after t = 0.  Time-block
+// summaries then describe each block scanned backwards, for blocks 1 .. nblocks-1.
+// ZOH: exact zero-order-hold input matrix (input_factor).
+template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS, bool SUMMARY, bool REV = false,
+          bool ZOH = false>
 __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
     selscan_fwd_seq_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
   using C = SeqCfg<NS, Q, R, Tin>;
@@ -225,7 +248,9 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   const bool row_ok = d < p.dim;
   const int N = FULLN ? NS : p.dstate;
   const int64_t L = p.seqlen;
-  const int kblk = blockIdx.z;  // time block: steps [tbeg, tend)
+  const int kslot = blockIdx.z;  // summary slot (summary pass) or time block (scan)
+  const int kblk = (SUMMARY && REV) ? kslot + 1 : kslot;  // time block: steps [tbeg, tend)
+  const int first_blk = REV ? p.nblocks - 1 : 0;         // the block that starts from h0
   const int64_t tbeg = static_cast<int64_t>(kblk) * p.tblock;
   const int64_t tend = (tbeg + p.tblock) < L ? (tbeg + p.tblock) : L;
   const int64_t c_begin = tbeg / T;               // tblock is a multiple of T
@@ -241,9 +266,10 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   // zero-filled and still count towards the expected bytes.
   const int row0 = static_cast<int>(b * p.dim + static_cast<int64_t>(blockIdx.x) * C::ROWS);
   const int ntens = SUMMARY ? 2 : (p.z ? 3 : 2);  // u, δ (, z)
-  // ci: chunk index within the time block (selects the buffer and the barrier phase).
+  // ci: chunk index within the time block in scan order (selects the buffer and the barrier phase).
+  auto chunk_of = [&](int64_t ci) { return REV ? c_begin + nchunks - 1 - ci : c_begin + ci; };
   auto issue = [&](int64_t ci) {
-    const int t0 = static_cast<int>((c_begin + ci) * T);
+    const int t0 = static_cast<int>(chunk_of(ci) * T);
     uint64_t* bar = &bars[ci & 1];
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_expect_tx(bar, static_cast<uint32_t>(((SUMMARY ? 1 : 2) * NS + ntens * C::ROWS) * T * sizeof(Tin)));
@@ -270,7 +296,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
 
   // This lane's states, in pairs: state n0 + 2i and n0 + 2i + 1.
   const int n0 = q * SPL;
-  float2 A2[PAIRS], h[PAIRS];
+  float2 A2[PAIRS], h[PAIRS], IA[PAIRS];
 #pragma unroll
   for (int i = 0; i < PAIRS; i++) {
     float a[2], hh[2];
@@ -281,13 +307,15 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
       a[k] = ok ? p.A[d * N + n] * kLog2e : 0.f;
       if (SUMMARY)
         hh[k] = 0.f;
-      else if (kblk > 0)
+      else if (kblk != first_blk)
         hh[k] = ok ? p.start[(kblk * rows_total + grow) * N + n] : 0.f;
       else
         hh[k] = (ok && p.h0) ? p.h0[grow * N + n] : 0.f;
     }
     A2[i] = f2(a[0], a[1]);
     h[i] = f2(hh[0], hh[1]);
+    // 1/A for the zero-order-hold factor (inf at A = 0, where the series branch is taken).
+    IA[i] = ZOH ? f2(kLog2e / a[0], kLog2e / a[1]) : f2(0.f, 0.f);
   }
   const float bias = (row_ok && p.delta_bias) ? p.delta_bias[d] : 0.f;
   const float Dd = (row_ok && p.D) ? p.D[d] : 0.f;
@@ -303,7 +331,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   float S = 0.f;  // Σ Δ over the block (summary pass)
   int64_t c = 0;  // chunk index within the time block
   for (; c < nchunks; c++) {
-    const int64_t t0 = (c_begin + c) * T;
+    const int64_t t0 = chunk_of(c) * T;
     const Tin* rb = raw + (c & 1) * C::RAW;
     float* tb = tiles + (c & 1) * C::TILE;
     const bool tail = t0 + T > L;
@@ -336,9 +364,13 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
     const unsigned char* sd = su + C::SUBT * C::ROWS * C::RB;
     const unsigned char* sz = sd + C::SUBT * C::ROWS * C::RB;
 #pragma unroll 1
-    for (int sb = 0; sb < T; sb += SB) {
+    for (int sbi = 0; sbi < T; sbi += SB) {
+      const int sb = REV ? T - SB - sbi : sbi;
       const int64_t ts = t0 + sb;
-      if (ts >= L) break;
+      if (ts >= L) {
+        if (REV) continue;  // sub-blocks past the end come first in reverse order
+        break;
+      }
       const bool full = !tail || ts + SB <= L;
       float dl[SB], du[SB], y[SB];
       Vec8<Tin> us_keep;  // this sub-block's u (the D skip is added after the state loop)
@@ -387,10 +419,11 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
           }
         }
       }
-      if (SUMMARY) {
+      if constexpr (SUMMARY) {
         // The block's end state from a zero start: the state recurrence only.
 #pragma unroll
-        for (int i = 0; i < SB; i++) {
+        for (int ii = 0; ii < SB; ii++) {
+          const int i = REV ? SB - 1 - ii : ii;
           const float2 dd = f2(dl[i], dl[i]), uu = f2(du[i], du[i]);
           const float4* bq = reinterpret_cast<const float4*>(tB + (sb + i) * TS);
 #pragma unroll
@@ -401,15 +434,16 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
               const int pi = 2 * g + k;
               const float2 e = mul2s(dd, A2[pi]);
               const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
-              h[pi] = fma2s(ab, h[pi], mul2s(uu, k ? f2(bb.z, bb.w) : f2(bb.x, bb.y)));
+              const float2 fu = input_factor<ZOH>(uu, e, ab, IA[pi], us_keep.get(i));
+              h[pi] = fma2s(ab, h[pi], mul2s(fu, k ? f2(bb.z, bb.w) : f2(bb.x, bb.y)));
             }
           }
         }
-        continue;
-      }
+      } else {
       float part[SB];
 #pragma unroll
-      for (int i = 0; i < SB; i++) {
+      for (int ii = 0; ii < SB; ii++) {
+        const int i = REV ? SB - 1 - ii : ii;
         const float2 dd = f2(dl[i], dl[i]), uu = f2(du[i], du[i]);
         const float4* bq = reinterpret_cast<const float4*>(tB + (sb + i) * TS);
         const float4* cq = reinterpret_cast<const float4*>(tC + (sb + i) * TS);
@@ -422,7 +456,8 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
             const int pi = 2 * g + k;
             const float2 e = mul2s(dd, A2[pi]);
             const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
-            h[pi] = fma2s(ab, h[pi], mul2s(uu, k ? f2(bb.z, bb.w) : f2(bb.x, bb.y)));
+            const float2 fu = input_factor<ZOH>(uu, e, ab, IA[pi], us_keep.get(i));
+            h[pi] = fma2s(ab, h[pi], mul2s(fu, k ? f2(bb.z, bb.w) : f2(bb.x, bb.y)));
             yp = fma2s(k ? f2(cc.z, cc.w) : f2(cc.x, cc.y), h[pi], yp);
           }
         }
@@ -466,6 +501,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
         }
         if (row_ok && q == 0) store8<Tout>(o_row, ts, L, vec && full, y);
       }
+      }  // scan (not summary)
     }
   }
 
@@ -479,7 +515,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   if (SUMMARY) {
     if constexpr (Q == 2) S += __shfl_xor_sync(kFull, S, RPW);  // each lane summed one half of the steps
     if (row_ok) {
-      float* o = p.summ + (kblk * rows_total + grow) * (N + 1);
+      float* o = p.summ + (kslot * rows_total + grow) * (N + 1);
 #pragma unroll
       for (int i = 0; i < PAIRS; i++)
 #pragma unroll
@@ -491,7 +527,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
     }
     return;
   }
-  if (row_ok && p.h_last && kblk == p.nblocks - 1) {
+  if (row_ok && p.h_last && kblk == (REV ? 0 : p.nblocks - 1)) {
 #pragma unroll
     for (int i = 0; i < PAIRS; i++)
 #pragma unroll
@@ -502,8 +538,10 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   }
 }
 
-// Start state of every time block from the blocks' summaries: for each (row, state), in block order,
-// s ← 2^(A·log2e·ΣΔ) s + (zero-start end state of the block).  Block 0 starts from h0.
+// Start state of every time block from the blocks' summaries: for each (row, state), in scan order,
+// s ← 2^(A·log2e·ΣΔ) s + (zero-start end state of the block).  The first block in scan order starts
+// from h0 (block 0, or with REV block nblocks-1, whose summaries sit in slots k-1 for blocks k >= 1).
+template <bool REV = false>
 __global__ void __launch_bounds__(256) selscan_carry_kernel(const FwdParams p) {
   const int64_t rows = p.batch * p.dim;
   const int N = p.dstate;
@@ -516,9 +554,12 @@ __global__ void __launch_bounds__(256) selscan_carry_kernel(const FwdParams p) {
   float st = p.h0 ? p.h0[grow * N + n] : 0.f;
 #pragma unroll 8
   for (int k = 0; k < p.nblocks - 1; k++) {
-    const float* sm = p.summ + (k * rows + grow) * (N + 1);
+    // Forward: summary slot k is block k and feeds block k+1.  Reverse: slot nblocks-2-k is block
+    // nblocks-1-k and feeds block nblocks-2-k.
+    const int slot = REV ? p.nblocks - 2 - k : k;
+    const float* sm = p.summ + (slot * rows + grow) * (N + 1);
     st = fmaf(ex2_approx(A2 * sm[N]), st, sm[n]);
-    p.start[((k + 1) * rows + grow) * N + n] = st;
+    p.start[((REV ? slot : k + 1) * rows + grow) * N + n] = st;
   }
 }
 
@@ -537,7 +578,8 @@ int64_t choose_tblock(const FwdParams& p, int64_t row_blocks, int slots) {
   return tb;
 }
 
-template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
+template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS, bool REV = false,
+          bool ZOH = false>
 cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
   using C = SeqCfg<NS, Q, R, Tin>;
   FwdParams p = p_in;
@@ -556,8 +598,8 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
               encode_2d<Tin>(enc, &maps.C, p.C, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE);
     p.use_tma = ok;
   }
-  auto scan = selscan_fwd_seq_kernel<NS, Q, R, Tin, Tout, FULLN, SOFTPLUS, false>;
-  auto summary = selscan_fwd_seq_kernel<NS, Q, R, Tin, float, FULLN, SOFTPLUS, true>;
+  auto scan = selscan_fwd_seq_kernel<NS, Q, R, Tin, Tout, FULLN, SOFTPLUS, false, REV, ZOH>;
+  auto summary = selscan_fwd_seq_kernel<NS, Q, R, Tin, float, FULLN, SOFTPLUS, true, REV, ZOH>;
   cudaError_t e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(summary, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
@@ -590,7 +632,7 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
   e = cudaGetLastError();
   if (e == cudaSuccess) {
     const int64_t threads = static_cast<int64_t>(rows) * N;
-    selscan_carry_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(p);
+    selscan_carry_kernel<REV><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(p);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
@@ -619,7 +661,39 @@ cudaError_t dispatch_seq(const FwdParams& p, cudaStream_t s) {
   return p.delta_softplus ? dispatch_seq_sp<Tin, Tout, true>(p, s) : dispatch_seq_sp<Tin, Tout, false>(p, s);
 }
 
+template <typename Tin, typename Tout, bool SOFTPLUS, bool REV, bool ZOH>
+cudaError_t dispatch_seq_ex_sp(const FwdParams& p, cudaStream_t s) {
+  constexpr int R = SELSCAN_SEQ_R;
+  if (p.dstate <= 4) return launch_seq_cfg<4, 1, R, Tin, Tout, false, SOFTPLUS, REV, ZOH>(p, s);
+  if (p.dstate <= 8) return launch_seq_cfg<8, 2, R, Tin, Tout, false, SOFTPLUS, REV, ZOH>(p, s);
+  return launch_seq_cfg<16, 2, R, Tin, Tout, false, SOFTPLUS, REV, ZOH>(p, s);
+}
+
+template <typename Tin, typename Tout, bool REV, bool ZOH>
+cudaError_t dispatch_seq_ex_flags(const FwdParams& p, cudaStream_t s) {
+  return p.delta_softplus ? dispatch_seq_ex_sp<Tin, Tout, true, REV, ZOH>(p, s)
+                          : dispatch_seq_ex_sp<Tin, Tout, false, REV, ZOH>(p, s);
+}
+
+template <typename Tin, typename Tout>
+cudaError_t dispatch_seq_ex(const FwdParams& p, bool reverse, bool zoh, cudaStream_t s) {
+  if (reverse && zoh) return dispatch_seq_ex_flags<Tin, Tout, true, true>(p, s);
+  if (reverse) return dispatch_seq_ex_flags<Tin, Tout, true, false>(p, s);
+  if (zoh) return dispatch_seq_ex_flags<Tin, Tout, false, true>(p, s);
+  return dispatch_seq<Tin, Tout>(p, s);
+}
+
 }  // namespace
+
+cudaError_t launch_fwd_seq_ex(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, bool reverse,
+                              bool zoh, cudaStream_t s) {
+  if (in_dtype == SELSCAN_F32) {
+    return out_dtype == SELSCAN_F32 ? dispatch_seq_ex<float, float>(p, reverse, zoh, s)
+                                    : dispatch_seq_ex<float, __nv_bfloat16>(p, reverse, zoh, s);
+  }
+  return out_dtype == SELSCAN_F32 ? dispatch_seq_ex<__nv_bfloat16, float>(p, reverse, zoh, s)
+                                  : dispatch_seq_ex<__nv_bfloat16, __nv_bfloat16>(p, reverse, zoh, s);
+}
 
 cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s) {
   if (in_dtype == SELSCAN_F32) {

@@ -89,6 +89,9 @@ inline bool encode_2d(EncodeTiled enc, CUtensorMap* m, const void* base, uint64_
 cudaError_t launch_step(const StepParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
 // The sequential forward kernel (rows-parallel, no scan) used by launch_fwd for many-row problems.
 cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
+// The sequential kernel in the reverse direction and/or with the exact zero-order-hold input matrix.
+cudaError_t launch_fwd_seq_ex(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, bool reverse,
+                              bool zoh, cudaStream_t s);
 // The sequential kernel with its time-block scratch in the library's fixed device array (no
 // allocation).  Sets *too_big and enqueues nothing if the problem needs more than the array holds.
 cudaError_t launch_fwd_seq_noalloc(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype,

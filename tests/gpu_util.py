@@ -35,6 +35,21 @@ def gpu_fwd(inp, delta_softplus=True, out_dtype="f32", h_last=True, stream=None,
     return out.float().cpu().numpy().astype(np.float64), (None if hl is None else hl.cpu().numpy().astype(np.float64))
 
 
+def gpu_fwd_ex(inp, reverse=False, zoh=False, delta_softplus=True, out_dtype="f32"):
+    """selscan_fwd_ex (reverse and/or exact zero-order hold) on an input dict; float64 numpy results."""
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    od = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    out, hl = ss.selscan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                                delta_bias=t["delta_bias"], delta_softplus=delta_softplus, h0=t["h0"],
+                                out_dtype=od, return_h_last=True, reverse=reverse, zoh=zoh)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64), hl.cpu().numpy().astype(np.float64)
+
+
 def tol_for(in_dtype):
     return FP32_TOL if in_dtype == "f32" else BF16_TOL
 

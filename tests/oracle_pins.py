@@ -20,6 +20,9 @@ Sources on the pages (by page title and section):
    Δ = softplus(· + param_Δ).
  * "Mamba状态空间模型深度解析" §2.1 — the selective SSM is a linear time-varying
    system (linear in its input and initial state for fixed Δ, B, C).
+ * "Mamba架构与SSM模型：高效序列建模技术解析" §2.1 — the zero-order hold that
+   discretises the continuous system h' = A h + B u (exact when the input is
+   held over each step), and §3.2 — a bidirectional (reverse-direction) option.
 """
 from __future__ import annotations
 
@@ -328,6 +331,108 @@ def pin_row_subset(lib):
     assert np.array_equal(sub, full.reshape(10, 19)[rows]) and np.array_equal(shl, hl.reshape(10, 3)[rows])
 
 
+def brute_force_reverse(inp, delta_softplus=True):
+    """The reverse-direction scan through its materialised anti-causal matrix.
+
+    Scanning from t = L-1 down to 0, h_t = Ā_t h_{t+1} + Δ_t B_t u_t with h_L = h0.  With the
+    exclusive prefix sum P_t = Σ_{r<t} Δ_r, ∏_{t≤r<s} Ā_r[n] = exp(A[n](P_s - P_t)), so
+      h_t[n] = Σ_{s≥t} exp(A[n](P_s - P_t)) Δ_s B_s[n] u_s + exp(A[n](P_L - P_t)) h0[n]
+    and y_t = Σ_n C_t[n] h_t[n] + D u_t (gated by silu(z)); h_last is h_0.
+    """
+    Bsz, Dm, L, N = inp["shape"]
+    u = np.asarray(inp["u"], np.float64)
+    x = np.asarray(inp["delta"], np.float64)
+    if inp.get("delta_bias") is not None:
+        x = x + np.asarray(inp["delta_bias"], np.float64)[None, :, None]
+    dt = _softplus_lib(x) if delta_softplus else x
+    Bm = np.asarray(inp["B"], np.float64)
+    Cm = np.asarray(inp["C"], np.float64)
+    A = np.asarray(inp["A"], np.float64)
+    Dv = np.zeros(Dm) if inp.get("D") is None else np.asarray(inp["D"], np.float64)
+    h0 = np.zeros((Bsz, Dm, N)) if inp.get("h0") is None else np.asarray(inp["h0"], np.float64)
+    out = np.zeros((Bsz, Dm, L))
+    hl = np.zeros((Bsz, Dm, N))
+    upper = np.triu(np.ones((L, L), dtype=bool))  # s >= t
+    for b in range(Bsz):
+        for d in range(Dm):
+            P = np.concatenate([[0.0], np.cumsum(dt[b, d])])  # P_0 .. P_L
+            y = Dv[d] * u[b, d].copy()
+            for n in range(N):
+                gap = np.where(upper, P[None, :L] - P[:L, None], 0.0)  # P_s - P_t for s >= t
+                decay = np.where(upper, np.exp(A[d, n] * gap), 0.0)
+                hn = decay @ (dt[b, d] * Bm[b, n] * u[b, d]) + np.exp(A[d, n] * (P[L] - P[:L])) * h0[b, d, n]
+                y += Cm[b, n] * hn
+                hl[b, d, n] = hn[0]
+            if inp.get("z") is not None:
+                zz = np.asarray(inp["z"], np.float64)[b, d]
+                y = y * zz * expit(zz)
+            out[b, d] = y
+    return out, hl
+
+
+def pin_reverse_brute_force(lib):
+    """Reverse-direction oracle == materialised anti-causal matrix (gate, bias, h0, D all on)."""
+    for seed, shape in [(81, (2, 3, 21, 3)), (82, (1, 2, 13, 1)), (83, (1, 2, 9, 5))]:
+        inp = _case(seed, *shape)
+        got, ghl = oracle.selscan_fwd(inp, reverse=True, lib=lib, nthreads=1)
+        want, whl = brute_force_reverse(inp)
+        _rel_close(got, want, 1e-11, what=f"reverse brute force out {shape}")
+        _rel_close(ghl, whl, 1e-11, what=f"reverse brute force h_last {shape}")
+
+
+def _rk4_zoh_reference(A, Bv, u, dt, h0, substeps=400):
+    """The continuous system h'(τ) = A h + B_t u_t, held constant over each interval of length Δ_t
+    (a zero-order hold of the input), integrated numerically with classical RK4."""
+    h = np.array(h0, dtype=np.float64)
+    hs = []
+    for t in range(len(dt)):
+        f = Bv[:, t] * u[t]
+        k = dt[t] / substeps
+        for _ in range(substeps):
+            k1 = A * h + f
+            k2 = A * (h + 0.5 * k * k1) + f
+            k3 = A * (h + 0.5 * k * k2) + f
+            k4 = A * (h + k * k3) + f
+            h = h + (k / 6.0) * (k1 + 2 * k2 + 2 * k3 + k4)
+        hs.append(h.copy())
+    return np.array(hs)  # [L, N]: state at the end of each interval
+
+
+def pin_zoh_matches_ode(lib):
+    """With zoh, the recurrence samples the continuous SSM exactly: each step advances the state of
+    h' = A h + B u over Δ_t with the input held constant, which RK4 reproduces to ~1e-10."""
+    Bsz, Dm, L, N = 1, 2, 12, 3
+    inp = _case(91, Bsz, Dm, L, N, has_z=False, has_bias=False)
+    inp["delta"] = (np.abs(inp["delta"]) * 0.7 + 0.05).astype(np.float32)  # Δ = δ (softplus off), 0.05..~2.5
+    got, hl = oracle.selscan_fwd(inp, delta_softplus=False, zoh=True, lib=lib, nthreads=1)
+    for d in range(Dm):
+        A = np.asarray(inp["A"][d], np.float64)
+        dt = np.asarray(inp["delta"][0, d], np.float64)
+        u = np.asarray(inp["u"][0, d], np.float64)
+        hs = _rk4_zoh_reference(A, np.asarray(inp["B"][0], np.float64), u, dt, inp["h0"][0, d])
+        y = (np.asarray(inp["C"][0], np.float64).T * hs).sum(1) + float(inp["D"][d]) * u
+        _rel_close(got[0, d], y, 1e-9, atol=1e-12, what="zoh out vs ODE")
+        _rel_close(hl[0, d], hs[-1], 1e-9, atol=1e-12, what="zoh h_last vs ODE")
+
+
+def pin_zoh_limits(lib):
+    """zoh at A = 0 is exactly the Δ·B scan (the limit of (e^{ΔA} - 1)/A), and for small Δ|A| the two
+    agree to first order: their difference shrinks like Δ²."""
+    inp = _case(92, 1, 3, 20, 4, has_z=False)
+    inp["A"] = np.zeros_like(inp["A"])
+    a, ah = oracle.selscan_fwd(inp, zoh=True, lib=lib, nthreads=1)
+    b, bh = oracle.selscan_fwd(inp, zoh=False, lib=lib, nthreads=1)
+    assert np.array_equal(a, b) and np.array_equal(ah, bh), "zoh at A = 0 must equal the Δ·B scan"
+    inp2 = _case(93, 1, 2, 8, 2, has_z=False, has_bias=False, has_h0=False)
+    diffs = []
+    for scale in (1e-2, 1e-3):
+        inp2["delta"] = np.full_like(inp2["delta"], scale)
+        z, _ = oracle.selscan_fwd(inp2, delta_softplus=False, zoh=True, lib=lib, nthreads=1)
+        e, _ = oracle.selscan_fwd(inp2, delta_softplus=False, zoh=False, lib=lib, nthreads=1)
+        diffs.append(np.max(np.abs(z - e)) / np.max(np.abs(e)))
+    assert 50 < diffs[0] / diffs[1] < 200, f"zoh minus Δ·B should shrink like Δ²: {diffs}"
+
+
 ALL_PINS = [pin_brute_force, pin_lti_convolution, pin_delta_to_zero, pin_prefix_sum, pin_memoryless, pin_gate,
             pin_scalar_functions, pin_carry, pin_step_equals_fwd, pin_linearity, pin_causality,
-            pin_worked_examples, pin_row_subset]
+            pin_worked_examples, pin_row_subset, pin_reverse_brute_force, pin_zoh_matches_ode, pin_zoh_limits]

@@ -106,6 +106,12 @@ def test_misaligned(lib, which, dt):
     assert _fwd(lib, _shape(i=dt), **{which: bad}) == 3
 
 
+def test_fwd_ex_rejects_unknown_flags(lib):
+    shape = _shape()
+    assert lib.selscan_fwd_ex(ctypes.byref(shape), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 1, None, FAKE,
+                              None, 4, None) == 4  # an unknown flag bit: SELSCAN_ERR_UNSUPPORTED
+
+
 def test_step_needs_seqlen_one(lib):
     assert _step(lib, _shape(L=2)) == 2
     assert _step(lib, _shape(L=1), state=None) == 1

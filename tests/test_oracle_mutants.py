@@ -16,12 +16,18 @@ from oracle_pins import ALL_PINS
 # (name, text in the oracle source, replacement); the text must occur exactly once
 MUTANTS = [
     ("sign_of_A", "exp(dt * a);", "exp(-dt * a);"),
-    ("drop_delta_in_Bbar", "abar * h[n] + dt * Bv * u;", "abar * h[n] + Bv * u;"),
+    ("drop_delta_in_Bbar", "? expm1(dt * a) / a : dt;", "? expm1(dt * a) / a : 1.0;"),
+    ("zoh_exp_not_expm1", "? expm1(dt * a) / a : dt;", "? exp(dt * a) / a : dt;"),
+    ("zoh_times_A", "? expm1(dt * a) / a : dt;", "? expm1(dt * a) * a : dt;"),
+    ("zoh_ignored", "(j->zoh && a != 0.0)", "(0 && a != 0.0)"),
+    ("zoh_missing_delta_limit", "(j->zoh && a != 0.0)", "(j->zoh)"),
+    ("reverse_ignored", "j->reverse ? (L - 1 - s) : s;", "s;"),
+    ("reverse_off_by_one", "j->reverse ? (L - 1 - s) : s;", "j->reverse ? (L - 1 - s + (s > 0)) : s;"),
     ("drop_D_term", "    y += Dd * u;\n", "\n"),
     ("read_state_before_update",
-     "      h[n] = abar * h[n] + dt * Bv * u;    /* h_t = Ā·h_{t-1} + Δ·B·u */\n"
+     "      h[n] = abar * h[n] + bbar * Bv * u;  /* h_t = Ā·h_{t-1} + B̄·u */\n"
      "      y += Cv * h[n];                      /* C·h_t reads the updated state */\n",
-     "      y += Cv * h[n];\n      h[n] = abar * h[n] + dt * Bv * u;\n"),
+     "      y += Cv * h[n];\n      h[n] = abar * h[n] + bbar * Bv * u;\n"),
     ("no_gate", "if (j->z) y *= silu(", "if (0) y *= silu("),
     ("gate_before_D", "    y += Dd * u;\n    if (j->z) y *= silu(load_in(j->z, e, j->in_dtype));\n",
      "    if (j->z) y *= silu(load_in(j->z, e, j->in_dtype));\n    y += Dd * u;\n"),

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import seeded_inputs as si
-from gpu_util import (check_h, check_out, decode_as_sequences, gpu_fwd, sample_rows, to_dev)
+from gpu_util import (check_h, check_out, decode_as_sequences, gpu_fwd, gpu_fwd_ex, sample_rows, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -138,6 +138,42 @@ def test_time_blocked_sequential(case, nblocks, monkeypatch):
     got, hl = gpu_fwd(inp, delta_softplus=sp)
     check_out(got, ref, dt)
     check_h(hl, href)
+
+
+# selscan_fwd_ex: the reverse direction and the exact zero-order-hold input matrix, alone and
+# together, in one pass and in time blocks, against the oracle run with the same options.
+EX_CASES = [
+    (51, 2, 5, 1000, 16, "bf16"),
+    (52, 1, 3, 777, 4, "f32"),
+    (53, 2, 6, 2049, 12, "f32"),
+]
+
+
+@pytest.mark.parametrize("opts", ["rev", "zoh", "rev_zoh", "none"])
+@pytest.mark.parametrize("nblocks", ["1", "3"])
+@pytest.mark.parametrize("case", EX_CASES, ids=[f"s{c[0]}_B{c[1]}D{c[2]}L{c[3]}N{c[4]}_{c[5]}" for c in EX_CASES])
+def test_fwd_ex_options(case, nblocks, opts, monkeypatch):
+    monkeypatch.setenv("SELSCAN_TBLOCKS", nblocks)
+    rev, zoh = "rev" in opts, "zoh" in opts
+    seed, Bsz, Dm, L, N, dt = case
+    inp = si.random_case(seed, Bsz, Dm, L, N, in_dtype=dt)
+    ref, href = oracle.selscan_fwd(inp, reverse=rev, zoh=zoh)
+    got, hl = gpu_fwd_ex(inp, reverse=rev, zoh=zoh)
+    check_out(got, ref, dt, what=f"fwd_ex {opts} out")
+    check_h(hl, href, what=f"fwd_ex {opts} h_last")
+
+
+@pytest.mark.parametrize("opts", ["rev", "zoh"])
+def test_fwd_ex_long_sequence_sampled(opts):
+    """The 65k-step workload (time blocks chosen by the library) in reverse and with exact ZOH."""
+    w = si.WORKLOADS["long_seq_65k"]
+    inp = si.make_inputs(w)
+    Bsz, Dm, L, N = inp["shape"]
+    got, hl = gpu_fwd_ex(inp, reverse=opts == "rev", zoh=opts == "zoh")
+    rows = sample_rows(Bsz, Dm, 8, seed=7)
+    ref, href = oracle.selscan_fwd(inp, rows=rows, reverse=opts == "rev", zoh=opts == "zoh")
+    check_out(got.reshape(Bsz * Dm, L)[rows], ref, w.in_dtype, what=f"long {opts} out")
+    check_h(hl.reshape(Bsz * Dm, N)[rows], href, what=f"long {opts} h_last")
 
 
 @pytest.mark.parametrize("name", ["mamba130m_layer", "long_seq_65k", "width_2p8b"])
