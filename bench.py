@@ -139,7 +139,7 @@ def max_over_ranks(seconds, dist, device):
 
 
 # The sources each kernel is built from (its own file and the shared device helpers).
-KERNEL_SOURCES = {"selscan_fwd": ("selscan_fwd.cu", "selscan_internal.cuh"),
+KERNEL_SOURCES = {"selscan_fwd": ("selscan_fwd.cu", "selscan_fwd_seq.cu", "selscan_internal.cuh"),
                   "selscan_step": ("selscan_step.cu", "selscan_internal.cuh")}
 
 
