@@ -43,8 +43,10 @@ def build() -> str:
 
 def _bind(lib):
     p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-    lib.oracle_selscan_fwd.argtypes = [i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p, i32, p, p, i32, i32, p, i64, p, p,
-                                       i32]
+    lib.oracle_selscan_fwd.argtypes = [i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p, i32, p, p, i32, i32, p, p, i64, p,
+                                       p, i32]
+    lib.oracle_conv_silu.argtypes = [i64, i64, i64, i64, i32, p, p, p, p]
+    lib.oracle_conv_silu.restype = i32
     lib.oracle_selscan_fwd.restype = i32
     lib.oracle_selscan_step.argtypes = [i64, i64, i64, i32, p, p, p, p, p, p, p, p, i32, p, p]
     lib.oracle_selscan_step.restype = i32
@@ -87,7 +89,7 @@ def _f32(a):
 
 def selscan_fwd(inp: Dict[str, object], delta_softplus: bool = True, rows: Optional[Sequence[int]] = None,
                 reverse: bool = False, nthreads: Optional[int] = None, h0_f64: Optional[np.ndarray] = None, lib=None,
-                zoh: bool = False):
+                zoh: bool = False, u_f64: Optional[np.ndarray] = None):
     """Run the fp64 forward on an input dict (see ``seeded_inputs.make_inputs``).
 
     Returns ``(out, h_last)`` as float64 arrays shaped ``[B, D, L]`` and
@@ -116,10 +118,24 @@ def selscan_fwd(inp: Dict[str, object], delta_softplus: bool = True, rows: Optio
                                 _ptr(D), _ptr(z), _ptr(bias), int(bool(delta_softplus)), _ptr(h0),
                                 _ptr(None if h0_f64 is None else np.ascontiguousarray(h0_f64, dtype=np.float64)),
                                 int(bool(reverse)), int(bool(zoh)),
+                                _ptr(None if u_f64 is None else np.ascontiguousarray(u_f64, dtype=np.float64)),
                                 rp, nr, _ptr(out), _ptr(hl), int(nth))
     if rc != 0:
         raise ValueError("oracle_selscan_fwd rejected its arguments")
     return out, hl
+
+
+def conv_silu(x, w, cb, in_dtype: str, lib=None) -> np.ndarray:
+    """u = silu(causal depthwise conv1d(x; w [D, K]) + cb) in fp64, for x [B, D, L] of ``in_dtype``."""
+    lib = lib or load()
+    xin = _in(x, in_dtype)
+    Bsz, Dm, L = xin.shape
+    w32 = np.ascontiguousarray(w, dtype=np.float32)
+    out = np.zeros((Bsz, Dm, L), dtype=np.float64)
+    rc = lib.oracle_conv_silu(Bsz, Dm, L, w32.shape[1], _DT[in_dtype], _ptr(xin), _ptr(w32), _ptr(_f32(cb)), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_conv_silu rejected its arguments")
+    return out
 
 
 def selscan_step(inp: Dict[str, object], state: np.ndarray, step: int = 0, delta_softplus: bool = True, lib=None):

@@ -78,6 +78,7 @@ typedef struct {
   const void *u, *delta, *z, *B, *C;
   const float *A, *D, *delta_bias, *h0;
   const double* h0_f64; /* fp64 start state; takes precedence over h0 */
+  const double* u_f64;  /* fp64 input [B, D, L]; takes precedence over u */
   int delta_softplus;
   int reverse; /* process t from L-1 down to 0 (bidirectional variant) */
   int zoh;     /* exact zero-order-hold input matrix instead of Δ·B */
@@ -104,7 +105,7 @@ static void scan_row(const fwd_job* j, int64_t b, int64_t d, double* out_row, do
   for (int64_t s = 0; s < L; s++) {
     const int64_t t = j->reverse ? (L - 1 - s) : s;
     const int64_t e = (b * Dm + d) * L + t; /* element index into [B, D, L] */
-    const double u = load_in(j->u, e, j->in_dtype);
+    const double u = j->u_f64 ? j->u_f64[e] : load_in(j->u, e, j->in_dtype);
     const double x = load_in(j->delta, e, j->in_dtype) + bias;
     const double dt = j->delta_softplus ? softplus(x) : x;
     double y = 0.0;
@@ -151,13 +152,13 @@ static void* fwd_worker(void* arg) {
 int oracle_selscan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype,
                        const void* u, const void* delta, const float* A, const void* B, const void* C,
                        const float* D, const void* z, const float* delta_bias, int delta_softplus,
-                       const float* h0, const double* h0_f64, int reverse, int zoh, const int64_t* rows,
-                       int64_t nrows,
+                       const float* h0, const double* h0_f64, int reverse, int zoh, const double* u_f64,
+                       const int64_t* rows, int64_t nrows,
                        double* out,
                        double* h_last, int nthreads) {
   if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1 || dstate > 64) return -1;
   if (in_dtype != ORACLE_F32 && in_dtype != ORACLE_BF16) return -1;
-  if (!u || !delta || !A || !B || !C || !out) return -1;
+  if ((!u && !u_f64) || !delta || !A || !B || !C || !out) return -1;
   fwd_job j;
   memset(&j, 0, sizeof j);
   j.batch = batch;
@@ -178,6 +179,7 @@ int oracle_selscan_fwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstat
   j.delta_softplus = delta_softplus;
   j.reverse = reverse;
   j.zoh = zoh;
+  j.u_f64 = u_f64;
   j.rows = rows;
   j.nrows = nrows;
   j.out = out;
@@ -234,6 +236,29 @@ int oracle_selscan_step(int64_t batch, int64_t dim, int64_t dstate, int in_dtype
 }
 
 /* Scalar helpers exposed for pinning the oracle's own building blocks. */
+/*
+ * The block's front before the scan: a causal depthwise 1-D convolution of width K over the
+ * sequence, plus a per-channel bias, then SiLU ("Mamba架构与SSM模型：高效序列建模技术解析" §3.2:
+ * d_conv = 4; "Mamba状态空间模型深度解析" §3.1: convolution then SiLU before the SSM):
+ *   u[b,d,t] = silu( cb[d] + Σ_{k=0}^{K-1} w[d,k] · x[b,d,t-(K-1)+k] ),   x[.., t<0] = 0.
+ * x is in_dtype [B, D, L]; w is fp32 [D, K]; cb is fp32 [D] or NULL.  Writes u in fp64.
+ */
+int oracle_conv_silu(int64_t batch, int64_t dim, int64_t seqlen, int64_t width, int in_dtype, const void* x,
+                     const float* w, const float* cb, double* u_out) {
+  if (batch < 0 || dim < 0 || seqlen < 0 || width < 1 || !x || !w || !u_out) return -1;
+  for (int64_t b = 0; b < batch; b++)
+    for (int64_t d = 0; d < dim; d++)
+      for (int64_t t = 0; t < seqlen; t++) {
+        double acc = cb ? (double)cb[d] : 0.0;
+        for (int64_t k = 0; k < width; k++) {
+          const int64_t tt = t - (width - 1) + k;
+          if (tt >= 0) acc += (double)w[d * width + k] * load_in(x, (b * dim + d) * seqlen + tt, in_dtype);
+        }
+        u_out[(b * dim + d) * seqlen + t] = silu(acc);
+      }
+  return 0;
+}
+
 double oracle_softplus(double x) { return softplus(x); }
 double oracle_silu(double z) { return silu(z); }
 double oracle_load_bf16(uint16_t bits) { return load_in(&bits, 0, ORACLE_BF16); }

@@ -433,6 +433,41 @@ def pin_zoh_limits(lib):
     assert 50 < diffs[0] / diffs[1] < 200, f"zoh minus Δ·B should shrink like Δ²: {diffs}"
 
 
+def pin_conv_silu(lib):
+    """The conv front against numpy's full convolution (first L outputs: causal, zero history) plus the
+    bias, and scipy's logistic for the SiLU: u = z·σ(z), z = cb + Σ_k w[k] x[t-3+k]."""
+    rng = np.random.default_rng(101)
+    Bsz, Dm, L, K = 2, 3, 37, 4
+    x = rng.standard_normal((Bsz, Dm, L)).astype(np.float32)
+    w = rng.standard_normal((Dm, K)).astype(np.float32)
+    cb = rng.standard_normal(Dm).astype(np.float32)
+    got = oracle.conv_silu(x, w, cb, "f32", lib=lib)
+    for b in range(Bsz):
+        for d in range(Dm):
+            zz = np.convolve(x[b, d].astype(np.float64), w[d, ::-1].astype(np.float64))[:L] + float(cb[d])
+            _rel_close(got[b, d], zz * expit(zz), 1e-13, atol=1e-15, what="conv+silu")
+    # an impulse at t0 reads the taps back in causal order: z_{t0+j} = w[K-1-j] for j < K, 0 after
+    imp = np.zeros((1, 1, 12), dtype=np.float32)
+    imp[0, 0, 5] = 1.0
+    wi = np.array([[0.25, -0.5, 2.0, 1.5]], dtype=np.float32)
+    gi = oracle.conv_silu(imp, wi, None, "f32", lib=lib)[0, 0]
+    zi = np.zeros(12)
+    zi[5:9] = [1.5, 2.0, -0.5, 0.25]
+    _rel_close(gi, zi * expit(zi), 1e-15, atol=1e-300, what="conv impulse response")
+
+
+def pin_conv_feeds_scan(lib):
+    """The scan with an fp64 u override equals the scan on that u stored in fp32 to fp32 rounding."""
+    inp = _case(102, 1, 2, 30, 3)
+    u64 = np.asarray(inp["u"], np.float64) * 0.5
+    inp32 = dict(inp)
+    inp32["u"] = u64.astype(np.float32)  # exact: halving an fp32 value only changes its exponent
+    a, ah = oracle.selscan_fwd(inp, u_f64=u64, lib=lib, nthreads=1)
+    b, bh = oracle.selscan_fwd(inp32, lib=lib, nthreads=1)
+    assert np.array_equal(a, b) and np.array_equal(ah, bh), "u_f64 must replace u exactly"
+
+
 ALL_PINS = [pin_brute_force, pin_lti_convolution, pin_delta_to_zero, pin_prefix_sum, pin_memoryless, pin_gate,
             pin_scalar_functions, pin_carry, pin_step_equals_fwd, pin_linearity, pin_causality,
-            pin_worked_examples, pin_row_subset, pin_reverse_brute_force, pin_zoh_matches_ode, pin_zoh_limits]
+            pin_worked_examples, pin_row_subset, pin_reverse_brute_force, pin_zoh_matches_ode, pin_zoh_limits,
+            pin_conv_silu, pin_conv_feeds_scan]

@@ -21,6 +21,11 @@ MUTANTS = [
     ("zoh_times_A", "? expm1(dt * a) / a : dt;", "? expm1(dt * a) * a : dt;"),
     ("zoh_ignored", "(j->zoh && a != 0.0)", "(0 && a != 0.0)"),
     ("zoh_missing_delta_limit", "(j->zoh && a != 0.0)", "(j->zoh)"),
+    ("conv_not_causal", "const int64_t tt = t - (width - 1) + k;", "const int64_t tt = t + k;"),
+    ("conv_taps_reversed", "acc += (double)w[d * width + k] * load_in", "acc += (double)w[d * width + width - 1 - k] * load_in"),
+    ("conv_bias_ignored", "double acc = cb ? (double)cb[d] : 0.0;", "double acc = 0.0;"),
+    ("conv_no_silu", "u_out[(b * dim + d) * seqlen + t] = silu(acc);", "u_out[(b * dim + d) * seqlen + t] = acc;"),
+    ("u_override_ignored", "const double u = j->u_f64 ? j->u_f64[e]", "const double u = 0 ? j->u_f64[e]"),
     ("reverse_ignored", "j->reverse ? (L - 1 - s) : s;", "s;"),
     ("reverse_off_by_one", "j->reverse ? (L - 1 - s) : s;", "j->reverse ? (L - 1 - s + (s > 0)) : s;"),
     ("drop_D_term", "    y += Dd * u;\n", "\n"),
@@ -46,8 +51,8 @@ MUTANTS = [
     ("D_index_wrong", "(double)j->D[d] : 0.0;", "(double)j->D[0] : 0.0;"),
     ("bias_index_wrong", "(double)j->delta_bias[d] : 0.0;\n  const double Dd",
      "(double)j->delta_bias[0] : 0.0;\n  const double Dd"),
-    ("u_index_off_by_one", "const double u = load_in(j->u, e, j->in_dtype);",
-     "const double u = load_in(j->u, t > 0 ? e - 1 : e, j->in_dtype);"),
+    ("u_index_off_by_one", "j->u_f64 ? j->u_f64[e] : load_in(j->u, e, j->in_dtype);",
+     "j->u_f64 ? j->u_f64[e] : load_in(j->u, t > 0 ? e - 1 : e, j->in_dtype);"),
     ("h_last_not_final", "for (int64_t n = 0; n < N; n++) hl_row[n] = h[n];",
      "for (int64_t n = 0; n < N; n++) hl_row[n] = 0.5 * h[n];"),
     ("step_sign_of_A", "*h = exp(dt * (double)A[d * dstate + n]) * (*h)", "*h = exp(-dt * (double)A[d * dstate + n]) * (*h)"),
