@@ -410,11 +410,21 @@ def run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world):
 
 
 def run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz, steps=50):
-    """Secondary: selscan_fwd_ex on the same workload with each option (reverse scan; exact
-    zero-order-hold input matrix), each step timed after an L2 flush, against the same roofline."""
+    """Secondary: the options on the same workload (selscan_fwd_ex's reverse scan and exact
+    zero-order-hold input matrix; selscan_fwd_conv's conv1d + SiLU front), each call timed after an
+    L2 flush, against the same roofline."""
     res = {}
-    for name, kw in (("reverse", dict(reverse=True)), ("zoh", dict(zoh=True))):
-        def call():
+    g = torch.Generator(device="cpu").manual_seed(5)
+    Dm = t["A"].shape[0]
+    conv_w = (torch.randn((Dm, 4), generator=g) * 0.5).to(t["A"].device)
+    conv_b = (torch.randn((Dm,), generator=g) * 0.5).to(t["A"].device)
+    for name, kw in (("reverse", dict(reverse=True)), ("zoh", dict(zoh=True)), ("conv", None)):
+        def call(kw=kw):
+            if kw is None:  # the causal conv1d + SiLU front computed in the kernel (u is read as x)
+                ss.selscan_fwd_conv(t["u"], conv_w, conv_b, t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                                    delta_bias=t["delta_bias"], delta_softplus=True, h0=t["h0"], out=out,
+                                    h_last=h_last, stream=stream)
+                return
             ss.selscan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
                               delta_bias=t["delta_bias"], delta_softplus=True, h0=t["h0"], out=out, h_last=h_last,
                               stream=stream, **kw)

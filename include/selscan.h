@@ -147,6 +147,31 @@ selscan_status_t selscan_fwd_ex(const selscan_shape_t* shape, const void* u, con
                                 float* h_last, unsigned flags, void* stream);
 
 /*
+ * Selective-scan forward with the block's convolution front computed in the kernel: u is not passed
+ * but computed from x by a causal depthwise 1-D convolution of width 4 and SiLU,
+ *
+ *   u[b,d,t] = silu( conv_b[d] + Σ_{k=0}^{3} conv_w[d,k] · x[b,d,t-3+k] ),   x before t = 0 is 0,
+ *
+ * and the scan then runs on u as in selscan_fwd (the D skip uses u).  ("Mamba架构与SSM模型：高效序列
+ * 建模技术解析" §3.2: d_conv = 4; "Mamba状态空间模型深度解析" §3.1: convolution then SiLU before the
+ * SSM.)  This saves writing u to memory and reading it back.
+ *
+ *   x       : [B, D, L]  in_dtype   the convolution's input (in place of u)
+ *   conv_w  : [D, 4]     fp32       taps; conv_w[d, 3] multiplies x_t, conv_w[d, 0] multiplies x_{t-3}
+ *   conv_b  : [D]        fp32       bias (nullable: 0)
+ *   flags   : 0 or SELSCAN_FLAG_ZOH (the front is causal: SELSCAN_FLAG_REVERSE is rejected with
+ *             SELSCAN_ERR_UNSUPPORTED)
+ * Every other argument, check and error is that of selscan_fwd.  A sequence split over calls
+ * restarts the convolution from zero history at each call's first step.  It runs the sequential
+ * kernel (with time blocks and their stream-ordered scratch for problems with few rows).
+ */
+selscan_status_t selscan_fwd_conv(const selscan_shape_t* shape, const void* x, const float* conv_w,
+                                  const float* conv_b, const void* delta, const float* A, const void* B,
+                                  const void* C, const float* D, const void* z, const float* delta_bias,
+                                  int delta_softplus, const float* h0, void* out, float* h_last, unsigned flags,
+                                  void* stream);
+
+/*
  * Selective-scan forward that allocates no memory at all: same arguments, layouts, validation and
  * result (within fp32 rounding) as selscan_fwd.  It is for callers that cannot call cudaMalloc or
  * cudaMallocAsync while they run, for example code that owns a fixed memory budget or that runs

@@ -22,7 +22,7 @@ STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SE
           4: "SELSCAN_ERR_UNSUPPORTED", 5: "SELSCAN_ERR_CUDA", 6: "SELSCAN_ERR_POINTER", 7: "SELSCAN_ERR_ALIAS",
           8: "SELSCAN_ERR_SCRATCH"}
 EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
-            "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex")
+            "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex", "selscan_fwd_conv")
 SELSCAN_FLAG_REVERSE, SELSCAN_FLAG_ZOH = 1, 2
 
 
@@ -58,6 +58,8 @@ def load_library(path: Optional[str] = None):
     lib.selscan_fwd.restype = i32
     lib.selscan_fwd_ex.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, ctypes.c_uint, vp]
     lib.selscan_fwd_ex.restype = i32
+    lib.selscan_fwd_conv.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, ctypes.c_uint, vp]
+    lib.selscan_fwd_conv.restype = i32
     lib.selscan_fwd_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
     lib.selscan_fwd_noalloc.restype = i32
     lib.selscan_step.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
@@ -204,6 +206,35 @@ def selscan_fwd_ex(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_sof
     return out, h_last
 
 
+def selscan_fwd_conv(x, conv_w, conv_b, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True,
+                     h0=None, out=None, h_last=None, stream=None, out_dtype=None, return_h_last: bool = False,
+                     zoh: bool = False):
+    """The forward with the convolution front: u = silu(conv_b + causal conv1d(x, conv_w [D, 4])),
+    computed in the kernel.  Other arguments and the return value as for ``selscan_fwd``."""
+    torch = _torch()
+    lib = load_library()
+    if x.dim() != 3 or B.dim() != 3:
+        raise ValueError("x must be [B, D, L] and B must be [B, N, L]")
+    Bsz, Dm, L = x.shape
+    N = B.shape[1]
+    for name, t in (("conv_w", conv_w), ("conv_b", conv_b), ("A", A), ("D", D), ("delta_bias", delta_bias),
+                    ("h0", h0), ("h_last", h_last)):
+        _need_f32(name, t)
+    for name, t in (("delta", delta), ("z", z), ("B", B), ("C", C)):
+        if t is not None and t.dtype != x.dtype:
+            raise TypeError(f"{name} must have x's dtype {x.dtype}")
+    if out is None:
+        out = torch.empty((Bsz, Dm, L), device=x.device, dtype=out_dtype or torch.float32)
+    if h_last is None and return_h_last:
+        h_last = torch.empty((Bsz, Dm, N), device=x.device, dtype=torch.float32)
+    shape = SelscanShape(Bsz, Dm, L, N, _dtype_code(x.dtype), _dtype_code(out.dtype))
+    st = lib.selscan_fwd_conv(ctypes.byref(shape), _ptr(x), _ptr(conv_w), _ptr(conv_b), _ptr(delta), _ptr(A), _ptr(B),
+                              _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0),
+                              _ptr(out), _ptr(h_last), SELSCAN_FLAG_ZOH if zoh else 0, _stream_handle(stream))
+    _check(st)
+    return out, h_last
+
+
 def selscan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
                         out=None, h_last=None, stream=None):
     """Selective-scan forward that allocates no device memory inside the library.
@@ -262,5 +293,5 @@ def selscan_step(u, delta, A, B, C, state, D=None, z=None, delta_bias=None, delt
     return out
 
 
-__all__ = ["selscan_fwd", "selscan_fwd_ex", "selscan_fwd_noalloc", "selscan_step", "selscan_status_string", "selscan_abi_version",
+__all__ = ["selscan_fwd", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step", "selscan_status_string", "selscan_abi_version",
            "selscan_last_cuda_error", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED"]

@@ -223,10 +223,16 @@ __device__ __forceinline__ float2 input_factor(float2 du, float2 e, float2 ab, f
 // sub-blocks and steps are taken in reverse order and h_last is the state after t = 0.  Time-block
 // summaries then describe each block scanned backwards, for blocks 1 .. nblocks-1.
 // ZOH: exact zero-order-hold input matrix (input_factor).
+// CONV: the input u is computed in the kernel from x (passed as `u`) by the block's convolution front,
+// u_t = silu(conv_b + Σ_{k<4} conv_w[k]·x_{t-3+k}) with x = 0 before t = 0 ("Mamba架构与SSM模型：
+// 高效序列建模技术解析" §3.2, d_conv = 4; "Mamba状态空间模型深度解析" §3.1, convolution and SiLU
+// before the SSM).  Each lane keeps the last three x of its row in registers; a time block reads
+// the three before its first step from memory.  Forward direction only.
 template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS, bool SUMMARY, bool REV = false,
-          bool ZOH = false>
+          bool ZOH = false, bool CONV = false>
 __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
     selscan_fwd_seq_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
+  static_assert(!(CONV && REV), "the convolution front is causal: forward direction only");
   using C = SeqCfg<NS, Q, R, Tin>;
   constexpr int T = C::T, SB = C::SB, TS = C::TS, SPL = C::SPL, PAIRS = C::PAIRS, RPW = C::RPW;
   extern __shared__ __align__(128) unsigned char smem_dyn[];
@@ -327,6 +333,19 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   const Tin* __restrict__ z_row = p.z ? static_cast<const Tin*>(p.z) + row_off : nullptr;
   Tout* __restrict__ o_row = static_cast<Tout*>(p.out) + row_off;
   const bool vec = p.vec_in && p.vec_out;
+  // Convolution front: taps, bias and the x history (x_{t-3}, x_{t-2}, x_{t-1}) before the block.
+  float cw0 = 0.f, cw1 = 0.f, cw2 = 0.f, cw3 = 0.f, cbias = 0.f, xm3 = 0.f, xm2 = 0.f, xm1 = 0.f;
+  if (CONV) {
+    const int64_t dd = row_ok ? d : 0;
+    cw0 = p.conv_w[dd * 4 + 0];
+    cw1 = p.conv_w[dd * 4 + 1];
+    cw2 = p.conv_w[dd * 4 + 2];
+    cw3 = p.conv_w[dd * 4 + 3];
+    cbias = p.conv_b ? p.conv_b[dd] : 0.f;
+    xm3 = tbeg >= 3 ? to_f32(u_row[tbeg - 3]) : 0.f;
+    xm2 = tbeg >= 2 ? to_f32(u_row[tbeg - 2]) : 0.f;
+    xm1 = tbeg >= 1 ? to_f32(u_row[tbeg - 1]) : 0.f;
+  }
 
   float S = 0.f;  // Σ Δ over the block (summary pass)
   int64_t c = 0;  // chunk index within the time block
@@ -373,16 +392,47 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
       }
       const bool full = !tail || ts + SB <= L;
       float dl[SB], du[SB], y[SB];
-      Vec8<Tin> us_keep;  // this sub-block's u (the D skip is added after the state loop)
+      float uval[SB];  // this sub-block's u (the D skip is added after the state loop)
       {
-        Vec8<Tin>& us = us_keep;
-        Vec8<Tin> ds;
+        Vec8<Tin> us, ds;
         if (tma) {
           stage8<Tin, C::ROWS, C::RB>(us, su, r_cta, sb);
           stage8<Tin, C::ROWS, C::RB>(ds, sd, r_cta, sb);
         } else {
           load8<Tin>(us, u_row, ts, L, vec && full);
           load8<Tin>(ds, dl_row, ts, L, vec && full);
+        }
+        if constexpr (CONV) {
+          float xv[SB], a[SB];
+#pragma unroll
+          for (int i = 0; i < SB; i++) xv[i] = us.get(i);
+#pragma unroll
+          for (int i = 0; i < SB; i++) {
+            const float x3 = i >= 3 ? xv[i - 3] : (i == 0 ? xm3 : (i == 1 ? xm2 : xm1));
+            const float x2 = i >= 2 ? xv[i - 2] : (i == 0 ? xm2 : xm1);
+            const float x1 = i >= 1 ? xv[i - 1] : xm1;
+            a[i] = fmaf(cw3, xv[i], fmaf(cw2, x1, fmaf(cw1, x2, fmaf(cw0, x3, cbias))));
+          }
+          xm3 = xv[SB - 3];
+          xm2 = xv[SB - 2];
+          xm1 = xv[SB - 1];
+          if constexpr (Q == 2) {
+            // Each lane of the row applies SiLU to one half of the steps and the halves are swapped.
+            constexpr int HB = SB / 2;
+            float mine[HB], other[HB];
+#pragma unroll
+            for (int m = 0; m < HB; m++) mine[m] = silu_fast(q ? a[HB + m] : a[m]);
+#pragma unroll
+            for (int m = 0; m < HB; m++) other[m] = __shfl_xor_sync(kFull, mine[m], RPW);
+#pragma unroll
+            for (int i = 0; i < SB; i++) uval[i] = ((i < HB) == (q == 0)) ? mine[i % HB] : other[i % HB];
+          } else {
+#pragma unroll
+            for (int i = 0; i < SB; i++) uval[i] = silu_fast(a[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < SB; i++) uval[i] = us.get(i);
         }
         if constexpr (Q == 2) {
           // The row's two lanes each compute Δ for one half of the 8 steps (lane q: steps
@@ -402,7 +452,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
           for (int i = 0; i < SB; i++) {
             const int m = i % HB;
             dl[i] = ((i < HB) == (q == 0)) ? mine[m] : other[m];
-            du[i] = dl[i] * us.get(i);
+            du[i] = dl[i] * uval[i];
           }
         } else {
           // Straight-line over the 8 steps (no branches), so their exponential/log chains overlap.
@@ -411,7 +461,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
             const float x = ds.get(i) + bias;
             float delta = SOFTPLUS ? softplus_fast(x) : x;
             delta = (full || ts + i < L) ? delta : 0.f;  // identity steps past the end
-            const float uu = us.get(i);
+            const float uu = uval[i];
             dl[i] = delta;
             du[i] = delta * uu;
             y[i] = Dd * uu;
@@ -434,7 +484,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
               const int pi = 2 * g + k;
               const float2 e = mul2s(dd, A2[pi]);
               const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
-              const float2 fu = input_factor<ZOH>(uu, e, ab, IA[pi], us_keep.get(i));
+              const float2 fu = input_factor<ZOH>(uu, e, ab, IA[pi], uval[i]);
               h[pi] = fma2s(ab, h[pi], mul2s(fu, k ? f2(bb.z, bb.w) : f2(bb.x, bb.y)));
             }
           }
@@ -456,7 +506,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
             const int pi = 2 * g + k;
             const float2 e = mul2s(dd, A2[pi]);
             const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
-            const float2 fu = input_factor<ZOH>(uu, e, ab, IA[pi], us_keep.get(i));
+            const float2 fu = input_factor<ZOH>(uu, e, ab, IA[pi], uval[i]);
             h[pi] = fma2s(ab, h[pi], mul2s(fu, k ? f2(bb.z, bb.w) : f2(bb.x, bb.y)));
             yp = fma2s(k ? f2(cc.z, cc.w) : f2(cc.x, cc.y), h[pi], yp);
           }
@@ -473,7 +523,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
           const float send = q ? part[m] : part[HB + m];
           const float keep = q ? part[HB + m] : part[m];
           yq[m] = keep + __shfl_xor_sync(kFull, send, RPW);
-          const float uu = q ? us_keep.get(HB + m) : us_keep.get(m);
+          const float uu = q ? uval[HB + m] : uval[m];
           yq[m] = fmaf(Dd, uu, yq[m]);
         }
         if (z_row) {
@@ -579,7 +629,7 @@ int64_t choose_tblock(const FwdParams& p, int64_t row_blocks, int slots) {
 }
 
 template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS, bool REV = false,
-          bool ZOH = false>
+          bool ZOH = false, bool CONV = false>
 cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
   using C = SeqCfg<NS, Q, R, Tin>;
   FwdParams p = p_in;
@@ -598,8 +648,8 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
               encode_2d<Tin>(enc, &maps.C, p.C, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE);
     p.use_tma = ok;
   }
-  auto scan = selscan_fwd_seq_kernel<NS, Q, R, Tin, Tout, FULLN, SOFTPLUS, false, REV, ZOH>;
-  auto summary = selscan_fwd_seq_kernel<NS, Q, R, Tin, float, FULLN, SOFTPLUS, true, REV, ZOH>;
+  auto scan = selscan_fwd_seq_kernel<NS, Q, R, Tin, Tout, FULLN, SOFTPLUS, false, REV, ZOH, CONV>;
+  auto summary = selscan_fwd_seq_kernel<NS, Q, R, Tin, float, FULLN, SOFTPLUS, true, REV, ZOH, CONV>;
   cudaError_t e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(summary, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
@@ -661,22 +711,25 @@ cudaError_t dispatch_seq(const FwdParams& p, cudaStream_t s) {
   return p.delta_softplus ? dispatch_seq_sp<Tin, Tout, true>(p, s) : dispatch_seq_sp<Tin, Tout, false>(p, s);
 }
 
-template <typename Tin, typename Tout, bool SOFTPLUS, bool REV, bool ZOH>
+template <typename Tin, typename Tout, bool SOFTPLUS, bool REV, bool ZOH, bool CONV = false>
 cudaError_t dispatch_seq_ex_sp(const FwdParams& p, cudaStream_t s) {
   constexpr int R = SELSCAN_SEQ_R;
-  if (p.dstate <= 4) return launch_seq_cfg<4, 1, R, Tin, Tout, false, SOFTPLUS, REV, ZOH>(p, s);
-  if (p.dstate <= 8) return launch_seq_cfg<8, 2, R, Tin, Tout, false, SOFTPLUS, REV, ZOH>(p, s);
-  return launch_seq_cfg<16, 2, R, Tin, Tout, false, SOFTPLUS, REV, ZOH>(p, s);
+  if (p.dstate <= 4) return launch_seq_cfg<4, 1, R, Tin, Tout, false, SOFTPLUS, REV, ZOH, CONV>(p, s);
+  if (p.dstate <= 8) return launch_seq_cfg<8, 2, R, Tin, Tout, false, SOFTPLUS, REV, ZOH, CONV>(p, s);
+  if (CONV && p.dstate == 16) return launch_seq_cfg<16, 2, R, Tin, Tout, true, SOFTPLUS, REV, ZOH, CONV>(p, s);
+  return launch_seq_cfg<16, 2, R, Tin, Tout, false, SOFTPLUS, REV, ZOH, CONV>(p, s);
 }
 
-template <typename Tin, typename Tout, bool REV, bool ZOH>
+template <typename Tin, typename Tout, bool REV, bool ZOH, bool CONV = false>
 cudaError_t dispatch_seq_ex_flags(const FwdParams& p, cudaStream_t s) {
-  return p.delta_softplus ? dispatch_seq_ex_sp<Tin, Tout, true, REV, ZOH>(p, s)
-                          : dispatch_seq_ex_sp<Tin, Tout, false, REV, ZOH>(p, s);
+  return p.delta_softplus ? dispatch_seq_ex_sp<Tin, Tout, true, REV, ZOH, CONV>(p, s)
+                          : dispatch_seq_ex_sp<Tin, Tout, false, REV, ZOH, CONV>(p, s);
 }
 
 template <typename Tin, typename Tout>
-cudaError_t dispatch_seq_ex(const FwdParams& p, bool reverse, bool zoh, cudaStream_t s) {
+cudaError_t dispatch_seq_ex(const FwdParams& p, bool reverse, bool zoh, cudaStream_t s, bool conv) {
+  if (conv) return zoh ? dispatch_seq_ex_flags<Tin, Tout, false, true, true>(p, s)
+                       : dispatch_seq_ex_flags<Tin, Tout, false, false, true>(p, s);
   if (reverse && zoh) return dispatch_seq_ex_flags<Tin, Tout, true, true>(p, s);
   if (reverse) return dispatch_seq_ex_flags<Tin, Tout, true, false>(p, s);
   if (zoh) return dispatch_seq_ex_flags<Tin, Tout, false, true>(p, s);
@@ -686,13 +739,14 @@ cudaError_t dispatch_seq_ex(const FwdParams& p, bool reverse, bool zoh, cudaStre
 }  // namespace
 
 cudaError_t launch_fwd_seq_ex(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, bool reverse,
-                              bool zoh, cudaStream_t s) {
+                              bool zoh, cudaStream_t s, bool conv) {
+  if (conv && reverse) return cudaErrorInvalidValue;  // the convolution front is causal
   if (in_dtype == SELSCAN_F32) {
-    return out_dtype == SELSCAN_F32 ? dispatch_seq_ex<float, float>(p, reverse, zoh, s)
-                                    : dispatch_seq_ex<float, __nv_bfloat16>(p, reverse, zoh, s);
+    return out_dtype == SELSCAN_F32 ? dispatch_seq_ex<float, float>(p, reverse, zoh, s, conv)
+                                    : dispatch_seq_ex<float, __nv_bfloat16>(p, reverse, zoh, s, conv);
   }
-  return out_dtype == SELSCAN_F32 ? dispatch_seq_ex<__nv_bfloat16, float>(p, reverse, zoh, s)
-                                  : dispatch_seq_ex<__nv_bfloat16, __nv_bfloat16>(p, reverse, zoh, s);
+  return out_dtype == SELSCAN_F32 ? dispatch_seq_ex<__nv_bfloat16, float>(p, reverse, zoh, s, conv)
+                                  : dispatch_seq_ex<__nv_bfloat16, __nv_bfloat16>(p, reverse, zoh, s, conv);
 }
 
 cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s) {

@@ -40,6 +40,9 @@ struct FwdParams {
   int nblocks;
   float* summ;
   float* start;
+  // Convolution front (selscan_fwd_conv): u = silu(conv_b + Σ_k conv_w[d,k]·x[t-3+k]); `u` then holds x.
+  const float* conv_w;  // [D, 4]
+  const float* conv_b;  // [D], nullable
 };
 
 // Arguments of one selscan_step launch.
@@ -89,9 +92,10 @@ inline bool encode_2d(EncodeTiled enc, CUtensorMap* m, const void* base, uint64_
 cudaError_t launch_step(const StepParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
 // The sequential forward kernel (rows-parallel, no scan) used by launch_fwd for many-row problems.
 cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
-// The sequential kernel in the reverse direction and/or with the exact zero-order-hold input matrix.
+// The sequential kernel in the reverse direction and/or with the exact zero-order-hold input matrix,
+// or (conv) with the causal conv1d + SiLU front computing u from x.
 cudaError_t launch_fwd_seq_ex(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, bool reverse,
-                              bool zoh, cudaStream_t s);
+                              bool zoh, cudaStream_t s, bool conv = false);
 // The sequential kernel with its time-block scratch in the library's fixed device array (no
 // allocation).  Sets *too_big and enqueues nothing if the problem needs more than the array holds.
 cudaError_t launch_fwd_seq_noalloc(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype,

@@ -50,6 +50,22 @@ def gpu_fwd_ex(inp, reverse=False, zoh=False, delta_softplus=True, out_dtype="f3
     return out.float().cpu().numpy().astype(np.float64), hl.cpu().numpy().astype(np.float64)
 
 
+def gpu_fwd_conv(inp, conv_w, conv_b, zoh=False, delta_softplus=True):
+    """selscan_fwd_conv with x = inp["u"] and the given taps and bias; float64 numpy results."""
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    w = torch.from_numpy(np.ascontiguousarray(conv_w, dtype=np.float32)).cuda()
+    cb = None if conv_b is None else torch.from_numpy(np.ascontiguousarray(conv_b, dtype=np.float32)).cuda()
+    out, hl = ss.selscan_fwd_conv(t["u"], w, cb, t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                                  delta_bias=t["delta_bias"], delta_softplus=delta_softplus, h0=t["h0"],
+                                  return_h_last=True, zoh=zoh)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64), hl.cpu().numpy().astype(np.float64)
+
+
 def tol_for(in_dtype):
     return FP32_TOL if in_dtype == "f32" else BF16_TOL
 

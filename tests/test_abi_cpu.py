@@ -112,6 +112,15 @@ def test_fwd_ex_rejects_unknown_flags(lib):
                               None, 4, None) == 4  # an unknown flag bit: SELSCAN_ERR_UNSUPPORTED
 
 
+def test_fwd_conv_rejects_reverse_and_missing_taps(lib):
+    shape = _shape()
+    # the front is causal: the reverse flag is refused before anything else is checked
+    assert lib.selscan_fwd_conv(ctypes.byref(shape), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None, None, 1,
+                                None, FAKE, None, 1, None) == 4
+    assert lib.selscan_fwd_conv(ctypes.byref(shape), FAKE, None, None, FAKE, FAKE, FAKE, FAKE, None, None, None, 1,
+                                None, FAKE, None, 0, None) == 1
+
+
 def test_step_needs_seqlen_one(lib):
     assert _step(lib, _shape(L=2)) == 2
     assert _step(lib, _shape(L=1), state=None) == 1

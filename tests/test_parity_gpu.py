@@ -14,7 +14,8 @@ import pytest
 
 import oracle
 import seeded_inputs as si
-from gpu_util import (check_h, check_out, decode_as_sequences, gpu_fwd, gpu_fwd_ex, sample_rows, to_dev)
+from gpu_util import (check_h, check_out, decode_as_sequences, gpu_fwd, gpu_fwd_conv, gpu_fwd_ex, sample_rows,
+                      to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -174,6 +175,60 @@ def test_fwd_ex_long_sequence_sampled(opts):
     ref, href = oracle.selscan_fwd(inp, rows=rows, reverse=opts == "rev", zoh=opts == "zoh")
     check_out(got.reshape(Bsz * Dm, L)[rows], ref, w.in_dtype, what=f"long {opts} out")
     check_h(hl.reshape(Bsz * Dm, N)[rows], href, what=f"long {opts} h_last")
+
+
+# selscan_fwd_conv: the causal conv1d (width 4) + SiLU front computed in the kernel from x, against
+# the oracle's conv front feeding its scan (u in fp64).
+def _conv_params(seed, Dm, with_bias=True):
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((Dm, 4)) * 0.5).astype(np.float32)
+    cb = (rng.standard_normal(Dm) * 0.5).astype(np.float32) if with_bias else None
+    return w, cb
+
+
+CONV_CASES = [
+    (61, 2, 5, 1000, 16, "bf16", True),
+    (62, 1, 3, 777, 4, "f32", False),
+    (63, 2, 6, 2049, 12, "f32", True),
+]
+
+
+@pytest.mark.parametrize("zoh", [False, True])
+@pytest.mark.parametrize("nblocks", ["1", "3"])
+@pytest.mark.parametrize("case", CONV_CASES, ids=[f"s{c[0]}_B{c[1]}D{c[2]}L{c[3]}N{c[4]}_{c[5]}" for c in CONV_CASES])
+def test_fwd_conv_front(case, nblocks, zoh, monkeypatch):
+    monkeypatch.setenv("SELSCAN_TBLOCKS", nblocks)
+    seed, Bsz, Dm, L, N, dt, with_bias = case
+    inp = si.random_case(seed, Bsz, Dm, L, N, in_dtype=dt)
+    w, cb = _conv_params(seed, Dm, with_bias)
+    u64 = oracle.conv_silu(inp["u"], w, cb, dt)
+    ref, href = oracle.selscan_fwd(inp, u_f64=u64, zoh=zoh)
+    got, hl = gpu_fwd_conv(inp, w, cb, zoh=zoh)
+    check_out(got, ref, dt, what="fwd_conv out")
+    check_h(hl, href, what="fwd_conv h_last")
+
+
+def test_fwd_conv_long_sequence_sampled():
+    """The 65k-step workload with the conv front (time blocks chosen by the library)."""
+    w_ = si.WORKLOADS["long_seq_65k"]
+    inp = si.make_inputs(w_)
+    Bsz, Dm, L, N = inp["shape"]
+    w, cb = _conv_params(64, Dm)
+    got, hl = gpu_fwd_conv(inp, w, cb)
+    assert Bsz == 1
+    ch = np.array(sample_rows(Bsz, Dm, 8, seed=9))
+    # The sampled channels as a problem of their own (batch 1, 8 channels) for the oracle.
+    sub = dict(inp)
+    for k in ("u", "delta", "z"):
+        sub[k] = None if inp.get(k) is None else np.ascontiguousarray(np.asarray(inp[k])[:, ch])
+    for k in ("A", "D", "delta_bias"):
+        sub[k] = None if inp.get(k) is None else np.ascontiguousarray(np.asarray(inp[k])[ch])
+    sub["h0"] = None if inp.get("h0") is None else np.ascontiguousarray(np.asarray(inp["h0"])[:, ch])
+    sub["shape"] = (1, len(ch), L, N)
+    u64 = oracle.conv_silu(sub["u"], w[ch], cb[ch], w_.in_dtype)
+    ref, href = oracle.selscan_fwd(sub, u_f64=u64)
+    check_out(got[:, ch], ref, w_.in_dtype, what="long conv out")
+    check_h(hl[:, ch], href, what="long conv h_last")
 
 
 @pytest.mark.parametrize("name", ["mamba130m_layer", "long_seq_65k", "width_2p8b"])
