@@ -14,7 +14,8 @@ Reported: ``value`` = elements (B·D·L) per second over all GPUs, from the
 per-step CUDA-event times summed over the K timed steps (max over ranks);
 ``hbm_gbs`` = algorithmic bytes / time; ``roofline`` for the fused forward
 kernel; ``e2e`` = the same metric with host (pinned) inputs copied in and the
-output copied back inside each timed step; ``cpu_baseline`` = the fp64 oracle
+output copied back for every step inside the timed region (steps pipelined
+over three streams: copies in, scan, copies out); ``cpu_baseline`` = the fp64 oracle
 on the host cores on a bounded row sample; ``decode`` = the recurrent decode
 step workload (secondary).  Under torchrun (N > 1) every rank runs its own
 shard of an N-times-larger batch (weak scaling, no data-path collective).
@@ -368,45 +369,72 @@ def run_ours(args, rank, world, local_rank, dist):
 
 
 def run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world):
-    """The same metric through the public API with pinned host buffers copied in and out each step."""
+    """The same metric through the public API with pinned host buffers copied in and out each step.
+
+    Steps are pipelined the way a stream of batches would be: the host->device copies of step k+1
+    (one stream), the scan of step k (the compute stream) and the device->host copies of step k-1
+    (a third stream) overlap, with two sets of device buffers ordered by events.  Every step still
+    moves its full inputs in and its full outputs out.
+    """
     Bsz, Dm, L, N = inp["shape"]
     names = ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")
     host = {k: _pinned(torch, inp.get(k)) for k in names}
-    dev = {k: (None if host[k] is None else torch.empty_like(host[k], device=device)) for k in names}
-    out = torch.empty((Bsz, Dm, L), device=device, dtype=torch.float32)
+    sets = [{k: (None if host[k] is None else torch.empty_like(host[k], device=device)) for k in names}
+            for _ in range(2)]
+    outs = [torch.empty((Bsz, Dm, L), device=device, dtype=torch.float32) for _ in range(2)]
+    hls = [torch.empty((Bsz, Dm, N), device=device, dtype=torch.float32) if w.returns_h_last else None
+           for _ in range(2)]
     out_h = torch.empty((Bsz, Dm, L), dtype=torch.float32).pin_memory()
-    hl = torch.empty((Bsz, Dm, N), device=device, dtype=torch.float32) if w.returns_h_last else None
     hl_h = torch.empty((Bsz, Dm, N), dtype=torch.float32).pin_memory() if w.returns_h_last else None
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = out_h.numel() * 4 + (hl_h.numel() * 4 if hl_h is not None else 0)
     steps = max(3, min(args.steps, args.e2e_steps))
+    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for e in comp_done + out_done:
+        e.record(stream)  # nothing outstanding at the start
 
-    def one():
-        for k in names:
-            if host[k] is not None:
-                dev[k].copy_(host[k], non_blocking=True)
+    def one(j):
+        k = j % 2
+        dev, out, hl = sets[k], outs[k], hls[k]
+        s_in.wait_event(comp_done[k])  # step j-2 has finished reading this input set
+        with torch.cuda.stream(s_in):
+            for n in names:
+                if host[n] is not None:
+                    dev[n].copy_(host[n], non_blocking=True)
+        in_done[k].record(s_in)
+        stream.wait_event(in_done[k])
+        stream.wait_event(out_done[k])  # step j-2's outputs have left this output set
         ss.selscan_fwd(dev["u"], dev["delta"], dev["A"], dev["B"], dev["C"], D=dev["D"], z=dev["z"],
                        delta_bias=dev["delta_bias"], h0=dev["h0"], out=out, h_last=hl, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        if hl is not None:
-            hl_h.copy_(hl, non_blocking=True)
+        comp_done[k].record(stream)
+        s_out.wait_event(comp_done[k])
+        with torch.cuda.stream(s_out):
+            out_h.copy_(out, non_blocking=True)
+            if hl is not None:
+                hl_h.copy_(hl, non_blocking=True)
+        out_done[k].record(s_out)
 
-    for _ in range(2):
-        one()
+    for j in range(2):
+        one(j)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     ev0.record(stream)
-    for _ in range(steps):
-        one()
+    s_in.wait_event(ev0)
+    for j in range(steps):
+        one(j)
+    stream.wait_stream(s_out)
+    stream.wait_stream(s_in)
     ev1.record(stream)
     torch.cuda.synchronize()
     secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist, device)
     return {"value": Bsz * Dm * L * steps * world / secs, "unit": "elems/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": secs / steps * 1e3,
-            "gpu_launches": steps}
+            "gpu_launches": steps, "pipelined": "h2d / scan / d2h on three streams, two buffer sets"}
 
 
 def run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz, steps=50):
