@@ -32,8 +32,9 @@
  *    arrays, last index fastest.  The caller owns every buffer.  The library
  *    keeps no state between calls; selscan_fwd takes stream-ordered scratch
  *    (cudaMallocAsync / cudaFreeAsync on `stream`) for the time blocks of
- *    problems with few rows (see selscan_fwd_noalloc for a variant that
- *    allocates nothing).
+ *    problems with few rows, and runs them in one pass instead if that
+ *    allocation fails (see selscan_fwd_noalloc for a variant that allocates
+ *    nothing).
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream).  A return of SELSCAN_OK means the work was
  *    enqueued; faults during execution surface at the caller's next

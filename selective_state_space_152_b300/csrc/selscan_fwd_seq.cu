@@ -669,12 +669,21 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
     return cudaGetLastError();
   }
   // Stream-ordered scratch for the block summaries and start states, released on the same stream.
+  // Time blocks only add parallelism: if the scratch cannot be had (no memory pool on the device, or
+  // the pool is exhausted), the same result (up to rounding) comes from one pass without it.
   const int64_t N = p.dstate;
   const size_t summ_floats = static_cast<size_t>(p.nblocks - 1) * rows * (N + 1);
   const size_t start_floats = static_cast<size_t>(p.nblocks) * rows * N;
   void* ws = nullptr;
   e = cudaMallocAsync(&ws, (summ_floats + start_floats) * sizeof(float), s);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // clear the allocation error
+    p.tblock = p.seqlen;
+    p.nblocks = 1;
+    const dim3 grid1(grid.x, grid.y, 1);
+    scan<<<grid1, R * 32, C::kSmem, s>>>(p, maps);
+    return cudaGetLastError();
+  }
   p.summ = static_cast<float*>(ws);
   p.start = p.summ + summ_floats;
   const dim3 sgrid(grid.x, grid.y, grid.z - 1);
