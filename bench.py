@@ -53,7 +53,7 @@ FALLBACK_SM_MHZ = 2032.0
 # ------------------------------------------------------------------------------------------------
 
 def measured_peaks(path=os.path.join(ROOT, "MEASURED_PEAKS.json")):
-    """(hbm GB/s, max SM MHz, source) from the generated peaks file, else the fallback."""
+    """(hbm GB/s, max SM MHz, source) from the measured-peaks file beside this script, else the fallback."""
     try:
         with open(path) as f:
             p = json.load(f)
