@@ -22,7 +22,9 @@ STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SE
           4: "SELSCAN_ERR_UNSUPPORTED", 5: "SELSCAN_ERR_CUDA", 6: "SELSCAN_ERR_POINTER", 7: "SELSCAN_ERR_ALIAS",
           8: "SELSCAN_ERR_SCRATCH"}
 EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
-            "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex", "selscan_fwd_conv")
+            "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_probe_rate")
+# Units of selscan_probe_rate (include/selscan_probe.h).
+PROBE_UNITS = {"ex2": 0, "lg2": 1, "rcp": 2, "tanh": 3, "ffma": 4, "ffma2": 5}
 SELSCAN_FLAG_REVERSE, SELSCAN_FLAG_ZOH = 1, 2
 
 
@@ -72,6 +74,8 @@ def load_library(path: Optional[str] = None):
     lib.selscan_device_status.restype = i32
     lib.selscan_abi_version.argtypes = []
     lib.selscan_abi_version.restype = i32
+    lib.selscan_probe_rate.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
+    lib.selscan_probe_rate.restype = i32
     if path is None:
         _lib = lib
     return lib
@@ -92,6 +96,17 @@ def selscan_last_cuda_error() -> int:
 def selscan_device_status(reset: bool = False) -> int:
     """0 if no kernel gave up a bounded wait since the last reset (synchronous read)."""
     return load_library().selscan_device_status(int(bool(reset)))
+
+
+def selscan_probe_rate(unit: str) -> float:
+    """Measured results per clock per SM of one arithmetic unit on the current device (synchronous).
+
+    ``unit`` is one of ``PROBE_UNITS``: "ex2", "lg2", "rcp", "tanh" (special-function unit), "ffma",
+    "ffma2" (fp32 FMA pipe, scalar and packed; fp32 results counted).
+    """
+    r = ctypes.c_double(0.0)
+    _check(load_library().selscan_probe_rate(PROBE_UNITS[unit], ctypes.byref(r)))
+    return r.value
 
 
 def _check(status: int):
@@ -293,5 +308,7 @@ def selscan_step(u, delta, A, B, C, state, D=None, z=None, delta_bias=None, delt
     return out
 
 
-__all__ = ["selscan_fwd", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step", "selscan_status_string", "selscan_abi_version",
-           "selscan_last_cuda_error", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED"]
+__all__ = ["selscan_fwd", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step",
+           "selscan_status_string", "selscan_abi_version", "selscan_last_cuda_error", "selscan_device_status",
+           "selscan_probe_rate", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED",
+           "PROBE_UNITS"]

@@ -29,7 +29,7 @@ NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC", f"
 # device code in parallel (--split-compile) cuts the clean build from about 8 to 2 minutes, and its
 # kernels measured as fast or faster.  The sequential kernel's file measured slower that way, so it
 # is compiled as one unit.
-FILE_FLAGS = {"selscan_fwd.cu": ["--split-compile=0"]}
+FILE_FLAGS = {"selscan_fwd.cu": ["--split-compile=0"], "selscan_rows.cu": ["--split-compile=0"]}
 
 
 def _nvcc() -> str:

@@ -3,6 +3,8 @@
 #include <cudaTypedefs.h>
 
 #include <climits>
+#include <cstdlib>
+#include <cstring>
 #include <cstdint>
 #include <mutex>
 
@@ -137,156 +139,18 @@ void* tensor_map_encoder() {
 }
 }  // namespace selscan
 
-extern "C" {
+namespace {
 
-selscan_status_t selscan_fwd(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
-                             const void* B, const void* C, const float* D, const void* z,
-                             const float* delta_bias, int delta_softplus, const float* h0, void* out,
-                             float* h_last, void* stream) {
-  selscan_status_t st = check_shape(shape);
-  if (st != SELSCAN_OK) return st;
-  const int64_t Bsz = shape->batch, Dm = shape->dim, L = shape->seqlen, N = shape->dstate;
-  int64_t rows, elems, bcn, bc_elems, an, states;
-  if (!mul_ok(Bsz, Dm, &rows) || !mul_ok(rows, L, &elems) || !mul_ok(Bsz, N, &bcn) || !mul_ok(bcn, L, &bc_elems) ||
-      !mul_ok(Dm, N, &an) || !mul_ok(rows, N, &states))
-    return SELSCAN_ERR_SHAPE;
-  if (elems > INT64_MAX / 4 || bc_elems > INT64_MAX / 4 || states > INT64_MAX / 4) return SELSCAN_ERR_SHAPE;
-  if (Bsz > 65535) return SELSCAN_ERR_UNSUPPORTED;  // one grid row per batch entry
-  const size_t ei = dsize(shape->in_dtype), eo = dsize(shape->out_dtype);
-  const Span ins[] = {{u, elems * (int64_t)ei},     {delta, elems * (int64_t)ei}, {A, an * 4},
-                      {B, bc_elems * (int64_t)ei},  {C, bc_elems * (int64_t)ei},  {D, Dm * 4},
-                      {z, elems * (int64_t)ei},     {delta_bias, Dm * 4},         {h0, states * 4}};
-  const bool req_in[] = {true, true, true, true, true, false, false, false, false};
-  const size_t el_in[] = {ei, ei, 4, ei, ei, 4, ei, 4, 4};
-  const Span outs[] = {{out, elems * (int64_t)eo}, {h_last, states * 4}};
-  const bool req_out[] = {true, false};
-  const size_t el_out[] = {eo, 4};
-  st = check_args(ins, req_in, el_in, 9, outs, req_out, el_out, 2, h0, h_last);
-  if (st != SELSCAN_OK) return st;
-  if (rows == 0) return SELSCAN_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (L == 0) {  // empty sequence: the state passes through unchanged
-    if (h_last && h_last != h0) {
-      cudaError_t e = h0 ? cudaMemcpyAsync(h_last, h0, states * 4, cudaMemcpyDeviceToDevice, s)
-                         : cudaMemsetAsync(h_last, 0, states * 4, s);
-      if (e != cudaSuccess) return cuda_fail(e);
-    }
-    return SELSCAN_OK;
-  }
-  selscan::FwdParams p;
-  p.batch = Bsz;
-  p.dim = Dm;
-  p.seqlen = L;
-  p.dstate = static_cast<int>(N);
-  p.u = u;
-  p.delta = delta;
-  p.z = z;
-  p.B = B;
-  p.C = C;
-  p.A = A;
-  p.D = D;
-  p.delta_bias = delta_bias;
-  p.h0 = h0;
-  p.out = out;
-  p.h_last = h_last;
-  p.delta_softplus = delta_softplus != 0;
-  const int64_t vin = 16 / ei, vout = 16 / eo;
-  p.vec_in = aligned(u, 16) && aligned(delta, 16) && (!z || aligned(z, 16)) && L % vin == 0;
-  p.vec_out = aligned(out, 16) && L % vout == 0;
-  p.vec_bc = aligned(B, 16) && aligned(C, 16) && L % vin == 0;
-  p.vec_stage = p.vec_bc && p.vec_in;  // u, delta, z rows may be bulk-copied too
-  p.use_tma = 0;
-  p.tblock = L;
-  p.nblocks = 1;
-  p.summ = nullptr;
-  p.start = nullptr;
-  p.conv_w = nullptr;
-  p.conv_b = nullptr;
-  cudaError_t e = selscan::launch_fwd(p, shape->in_dtype, shape->out_dtype, s);
-  return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
-}
-
-// selscan_fwd with the reverse direction and/or the exact zero-order-hold input matrix: the same
-// checks, then the sequential kernel instantiated for the requested options.
-selscan_status_t selscan_fwd_ex(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
-                                const void* B, const void* C, const float* D, const void* z,
-                                const float* delta_bias, int delta_softplus, const float* h0, void* out,
-                                float* h_last, unsigned flags, void* stream) {
-  if (flags & ~(SELSCAN_FLAG_REVERSE | SELSCAN_FLAG_ZOH)) return SELSCAN_ERR_UNSUPPORTED;
-  selscan_status_t st = check_shape(shape);
-  if (st != SELSCAN_OK) return st;
-  const int64_t Bsz = shape->batch, Dm = shape->dim, L = shape->seqlen, N = shape->dstate;
-  int64_t rows, elems, bcn, bc_elems, an, states;
-  if (!mul_ok(Bsz, Dm, &rows) || !mul_ok(rows, L, &elems) || !mul_ok(Bsz, N, &bcn) || !mul_ok(bcn, L, &bc_elems) ||
-      !mul_ok(Dm, N, &an) || !mul_ok(rows, N, &states))
-    return SELSCAN_ERR_SHAPE;
-  if (elems > INT64_MAX / 4 || bc_elems > INT64_MAX / 4 || states > INT64_MAX / 4) return SELSCAN_ERR_SHAPE;
-  if (Bsz > 65535) return SELSCAN_ERR_UNSUPPORTED;  // one grid row per batch entry
-  const size_t ei = dsize(shape->in_dtype), eo = dsize(shape->out_dtype);
-  const Span ins[] = {{u, elems * (int64_t)ei},     {delta, elems * (int64_t)ei}, {A, an * 4},
-                      {B, bc_elems * (int64_t)ei},  {C, bc_elems * (int64_t)ei},  {D, Dm * 4},
-                      {z, elems * (int64_t)ei},     {delta_bias, Dm * 4},         {h0, states * 4}};
-  const bool req_in[] = {true, true, true, true, true, false, false, false, false};
-  const size_t el_in[] = {ei, ei, 4, ei, ei, 4, ei, 4, 4};
-  const Span outs[] = {{out, elems * (int64_t)eo}, {h_last, states * 4}};
-  const bool req_out[] = {true, false};
-  const size_t el_out[] = {eo, 4};
-  st = check_args(ins, req_in, el_in, 9, outs, req_out, el_out, 2, h0, h_last);
-  if (st != SELSCAN_OK) return st;
-  if (rows == 0) return SELSCAN_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (L == 0) {  // empty sequence: the state passes through unchanged
-    if (h_last && h_last != h0) {
-      cudaError_t e = h0 ? cudaMemcpyAsync(h_last, h0, states * 4, cudaMemcpyDeviceToDevice, s)
-                         : cudaMemsetAsync(h_last, 0, states * 4, s);
-      if (e != cudaSuccess) return cuda_fail(e);
-    }
-    return SELSCAN_OK;
-  }
-  selscan::FwdParams p;
-  p.batch = Bsz;
-  p.dim = Dm;
-  p.seqlen = L;
-  p.dstate = static_cast<int>(N);
-  p.u = u;
-  p.delta = delta;
-  p.z = z;
-  p.B = B;
-  p.C = C;
-  p.A = A;
-  p.D = D;
-  p.delta_bias = delta_bias;
-  p.h0 = h0;
-  p.out = out;
-  p.h_last = h_last;
-  p.delta_softplus = delta_softplus != 0;
-  const int64_t vin = 16 / ei, vout = 16 / eo;
-  p.vec_in = aligned(u, 16) && aligned(delta, 16) && (!z || aligned(z, 16)) && L % vin == 0;
-  p.vec_out = aligned(out, 16) && L % vout == 0;
-  p.vec_bc = aligned(B, 16) && aligned(C, 16) && L % vin == 0;
-  p.vec_stage = p.vec_bc && p.vec_in;  // u, delta, z rows may be bulk-copied too
-  p.use_tma = 0;
-  p.tblock = L;
-  p.nblocks = 1;
-  p.summ = nullptr;
-  p.start = nullptr;
-  p.conv_w = nullptr;
-  p.conv_b = nullptr;
-  cudaError_t e = selscan::launch_fwd_seq_ex(p, shape->in_dtype, shape->out_dtype, (flags & SELSCAN_FLAG_REVERSE) != 0,
-                                             (flags & SELSCAN_FLAG_ZOH) != 0, s);
-  return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
-}
-
-// The forward with the block's convolution front: u = silu(conv_b + causal depthwise conv1d(x, conv_w)),
-// computed in the sequential kernel from x (passed where selscan_fwd takes u).  The checks of
-// selscan_fwd, plus conv_w [D, 4] fp32 (required) and conv_b [D] fp32 (optional).
-selscan_status_t selscan_fwd_conv(const selscan_shape_t* shape, const void* u, const float* conv_w,
-                                  const float* conv_b, const void* delta, const float* A, const void* B,
-                                  const void* C, const float* D, const void* z, const float* delta_bias,
-                                  int delta_softplus, const float* h0, void* out, float* h_last, unsigned flags,
-                                  void* stream) {
-  if (flags & ~SELSCAN_FLAG_ZOH) return SELSCAN_ERR_UNSUPPORTED;  // the front is causal: no reverse
-  if (!conv_w) return SELSCAN_ERR_NULL;
+// The checks shared by every forward entry point, and the launch arguments they produce.  *done is set
+// when nothing is left to launch: no rows, or an empty sequence (h_last = h0 or zeros, written here
+// by a copy or a fill, which allocate nothing).
+selscan_status_t prepare_fwd(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                             const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                             int delta_softplus, const float* h0, void* out, float* h_last, bool conv,
+                             const float* conv_w, const float* conv_b, cudaStream_t s, selscan::FwdParams* p,
+                             bool* done) {
+  *done = false;
+  if (conv && !conv_w) return SELSCAN_ERR_NULL;
   selscan_status_t st = check_shape(shape);
   if (st != SELSCAN_OK) return st;
   const int64_t Bsz = shape->batch, Dm = shape->dim, L = shape->seqlen, N = shape->dstate;
@@ -300,17 +164,20 @@ selscan_status_t selscan_fwd_conv(const selscan_shape_t* shape, const void* u, c
   const Span ins[] = {{u, elems * (int64_t)ei},     {delta, elems * (int64_t)ei}, {A, an * 4},
                       {B, bc_elems * (int64_t)ei},  {C, bc_elems * (int64_t)ei},  {D, Dm * 4},
                       {z, elems * (int64_t)ei},     {delta_bias, Dm * 4},         {h0, states * 4},
-                      {conv_w, Dm * 16},            {conv_b, Dm * 4}};
-  const bool req_in[] = {true, true, true, true, true, false, false, false, false, true, false};
+                      {conv ? conv_w : nullptr, Dm * 16}, {conv ? conv_b : nullptr, Dm * 4}};
+  const bool req_in[] = {true, true, true, true, true, false, false, false, false, conv, false};
   const size_t el_in[] = {ei, ei, 4, ei, ei, 4, ei, 4, 4, 4, 4};
   const Span outs[] = {{out, elems * (int64_t)eo}, {h_last, states * 4}};
   const bool req_out[] = {true, false};
   const size_t el_out[] = {eo, 4};
   st = check_args(ins, req_in, el_in, 11, outs, req_out, el_out, 2, h0, h_last);
   if (st != SELSCAN_OK) return st;
-  if (rows == 0) return SELSCAN_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (rows == 0) {
+    *done = true;
+    return SELSCAN_OK;
+  }
   if (L == 0) {  // empty sequence: the state passes through unchanged
+    *done = true;
     if (h_last && h_last != h0) {
       cudaError_t e = h0 ? cudaMemcpyAsync(h_last, h0, states * 4, cudaMemcpyDeviceToDevice, s)
                          : cudaMemsetAsync(h_last, 0, states * 4, s);
@@ -318,107 +185,134 @@ selscan_status_t selscan_fwd_conv(const selscan_shape_t* shape, const void* u, c
     }
     return SELSCAN_OK;
   }
-  selscan::FwdParams p;
-  p.batch = Bsz;
-  p.dim = Dm;
-  p.seqlen = L;
-  p.dstate = static_cast<int>(N);
-  p.u = u;
-  p.delta = delta;
-  p.z = z;
-  p.B = B;
-  p.C = C;
-  p.A = A;
-  p.D = D;
-  p.delta_bias = delta_bias;
-  p.h0 = h0;
-  p.out = out;
-  p.h_last = h_last;
-  p.delta_softplus = delta_softplus != 0;
+  memset(p, 0, sizeof *p);
+  p->batch = Bsz;
+  p->dim = Dm;
+  p->seqlen = L;
+  p->dstate = static_cast<int>(N);
+  p->u = u;
+  p->delta = delta;
+  p->z = z;
+  p->B = B;
+  p->C = C;
+  p->A = A;
+  p->D = D;
+  p->delta_bias = delta_bias;
+  p->h0 = h0;
+  p->out = out;
+  p->h_last = h_last;
+  p->delta_softplus = delta_softplus != 0;
   const int64_t vin = 16 / ei, vout = 16 / eo;
-  p.vec_in = aligned(u, 16) && aligned(delta, 16) && (!z || aligned(z, 16)) && L % vin == 0;
-  p.vec_out = aligned(out, 16) && L % vout == 0;
-  p.vec_bc = aligned(B, 16) && aligned(C, 16) && L % vin == 0;
-  p.vec_stage = p.vec_bc && p.vec_in;  // u, delta, z rows may be bulk-copied too
-  p.use_tma = 0;
-  p.tblock = L;
-  p.nblocks = 1;
-  p.summ = nullptr;
-  p.start = nullptr;
-  p.conv_w = conv_w;
-  p.conv_b = conv_b;
-  cudaError_t e = selscan::launch_fwd_seq_ex(p, shape->in_dtype, shape->out_dtype, false,
-                                             (flags & SELSCAN_FLAG_ZOH) != 0, s, true);
+  p->vec_in = aligned(u, 16) && aligned(delta, 16) && (!z || aligned(z, 16)) && L % vin == 0;
+  p->vec_out = aligned(out, 16) && L % vout == 0;
+  p->vec_bc = aligned(B, 16) && aligned(C, 16) && L % vin == 0;
+  p->vec_stage = p->vec_bc && p->vec_in;  // u, delta, z rows may be bulk-copied too
+  p->tblock = L;
+  p->nblocks = 1;
+  p->conv_w = conv ? conv_w : nullptr;
+  p->conv_b = conv ? conv_b : nullptr;
+  p->out_bf16 = shape->out_dtype == SELSCAN_BF16;
+  return SELSCAN_OK;
+}
+
+// The row-sequential kernel unless it cannot stage the inputs or SELSCAN_KERNEL forces an older one.
+bool rows_path(const selscan::FwdParams& p, selscan_dtype_t in_dtype) {
+  const char* k = getenv("SELSCAN_KERNEL");
+  return (!k || k[0] == 'r') && selscan::rows_kernel_supports(p, in_dtype);
+}
+
+}  // namespace
+
+extern "C" {
+
+selscan_status_t selscan_fwd(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* delta_bias, int delta_softplus, const float* h0, void* out,
+                             float* h_last, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  selscan::FwdParams p;
+  bool done = false;
+  selscan_status_t st = prepare_fwd(shape, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, out, h_last,
+                                    false, nullptr, nullptr, s, &p, &done);
+  if (st != SELSCAN_OK || done) return st;
+  cudaError_t e = selscan::launch_fwd(p, shape->in_dtype, shape->out_dtype, s);
   return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
 }
 
-// For callers that may not allocate device memory while they run: the same checks as selscan_fwd,
-// then the sequential kernel with its time-block scratch in the library's fixed device array.
+// selscan_fwd with the reverse direction and/or the exact zero-order-hold input matrix.
+selscan_status_t selscan_fwd_ex(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                                const void* B, const void* C, const float* D, const void* z,
+                                const float* delta_bias, int delta_softplus, const float* h0, void* out,
+                                float* h_last, unsigned flags, void* stream) {
+  if (flags & ~(SELSCAN_FLAG_REVERSE | SELSCAN_FLAG_ZOH)) return SELSCAN_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  selscan::FwdParams p;
+  bool done = false;
+  selscan_status_t st = prepare_fwd(shape, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, out, h_last,
+                                    false, nullptr, nullptr, s, &p, &done);
+  if (st != SELSCAN_OK || done) return st;
+  const bool rev = (flags & SELSCAN_FLAG_REVERSE) != 0, zoh = (flags & SELSCAN_FLAG_ZOH) != 0;
+  cudaError_t e;
+  if (rows_path(p, shape->in_dtype)) {
+    selscan::RowsOptions o;
+    o.reverse = rev;
+    o.zoh = zoh;
+    e = selscan::launch_fwd_rows(p, shape->in_dtype, shape->out_dtype, o, s, nullptr);
+  } else {
+    e = selscan::launch_fwd_seq_ex(p, shape->in_dtype, shape->out_dtype, rev, zoh, s);
+  }
+  return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
+}
+
+// The forward with the block's convolution front: u = silu(conv_b + causal depthwise conv1d(x, conv_w)),
+// computed in the kernel from x (passed where selscan_fwd takes u).  The checks of selscan_fwd, plus
+// conv_w [D, 4] fp32 (required) and conv_b [D] fp32 (optional).
+selscan_status_t selscan_fwd_conv(const selscan_shape_t* shape, const void* u, const float* conv_w,
+                                  const float* conv_b, const void* delta, const float* A, const void* B,
+                                  const void* C, const float* D, const void* z, const float* delta_bias,
+                                  int delta_softplus, const float* h0, void* out, float* h_last, unsigned flags,
+                                  void* stream) {
+  if (flags & ~SELSCAN_FLAG_ZOH) return SELSCAN_ERR_UNSUPPORTED;  // the front is causal: no reverse
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  selscan::FwdParams p;
+  bool done = false;
+  selscan_status_t st = prepare_fwd(shape, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, out, h_last,
+                                    true, conv_w, conv_b, s, &p, &done);
+  if (st != SELSCAN_OK || done) return st;
+  const bool zoh = (flags & SELSCAN_FLAG_ZOH) != 0;
+  cudaError_t e;
+  if (rows_path(p, shape->in_dtype)) {
+    selscan::RowsOptions o;
+    o.zoh = zoh;
+    o.conv = true;
+    e = selscan::launch_fwd_rows(p, shape->in_dtype, shape->out_dtype, o, s, nullptr);
+  } else {
+    e = selscan::launch_fwd_seq_ex(p, shape->in_dtype, shape->out_dtype, false, zoh, s, true);
+  }
+  return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
+}
+
+// For callers that may not allocate device memory while they run: the checks of selscan_fwd, then the
+// forward with its time-block scratch in the library's fixed device array.
 selscan_status_t selscan_fwd_noalloc(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
                                      const void* B, const void* C, const float* D, const void* z,
                                      const float* delta_bias, int delta_softplus, const float* h0, void* out,
                                      float* h_last, void* stream) {
-  selscan_status_t st = check_shape(shape);
-  if (st != SELSCAN_OK) return st;
-  const int64_t Bsz = shape->batch, Dm = shape->dim, L = shape->seqlen, N = shape->dstate;
-  int64_t rows, elems, bcn, bc_elems, an, states;
-  if (!mul_ok(Bsz, Dm, &rows) || !mul_ok(rows, L, &elems) || !mul_ok(Bsz, N, &bcn) || !mul_ok(bcn, L, &bc_elems) ||
-      !mul_ok(Dm, N, &an) || !mul_ok(rows, N, &states))
-    return SELSCAN_ERR_SHAPE;
-  if (elems > INT64_MAX / 4 || bc_elems > INT64_MAX / 4 || states > INT64_MAX / 4) return SELSCAN_ERR_SHAPE;
-  if (Bsz > 65535) return SELSCAN_ERR_UNSUPPORTED;  // one grid row per batch entry
-  const size_t ei = dsize(shape->in_dtype), eo = dsize(shape->out_dtype);
-  const Span ins[] = {{u, elems * (int64_t)ei},     {delta, elems * (int64_t)ei}, {A, an * 4},
-                      {B, bc_elems * (int64_t)ei},  {C, bc_elems * (int64_t)ei},  {D, Dm * 4},
-                      {z, elems * (int64_t)ei},     {delta_bias, Dm * 4},         {h0, states * 4}};
-  const bool req_in[] = {true, true, true, true, true, false, false, false, false};
-  const size_t el_in[] = {ei, ei, 4, ei, ei, 4, ei, 4, 4};
-  const Span outs[] = {{out, elems * (int64_t)eo}, {h_last, states * 4}};
-  const bool req_out[] = {true, false};
-  const size_t el_out[] = {eo, 4};
-  st = check_args(ins, req_in, el_in, 9, outs, req_out, el_out, 2, h0, h_last);
-  if (st != SELSCAN_OK) return st;
-  if (rows == 0) return SELSCAN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (L == 0) {  // empty sequence: the state passes through unchanged (a copy or a fill, no allocation)
-    if (h_last && h_last != h0) {
-      cudaError_t e = h0 ? cudaMemcpyAsync(h_last, h0, states * 4, cudaMemcpyDeviceToDevice, s)
-                         : cudaMemsetAsync(h_last, 0, states * 4, s);
-      if (e != cudaSuccess) return cuda_fail(e);
-    }
-    return SELSCAN_OK;
-  }
   selscan::FwdParams p;
-  p.batch = Bsz;
-  p.dim = Dm;
-  p.seqlen = L;
-  p.dstate = static_cast<int>(N);
-  p.u = u;
-  p.delta = delta;
-  p.z = z;
-  p.B = B;
-  p.C = C;
-  p.A = A;
-  p.D = D;
-  p.delta_bias = delta_bias;
-  p.h0 = h0;
-  p.out = out;
-  p.h_last = h_last;
-  p.delta_softplus = delta_softplus != 0;
-  const int64_t vin = 16 / ei, vout = 16 / eo;
-  p.vec_in = aligned(u, 16) && aligned(delta, 16) && (!z || aligned(z, 16)) && L % vin == 0;
-  p.vec_out = aligned(out, 16) && L % vout == 0;
-  p.vec_bc = aligned(B, 16) && aligned(C, 16) && L % vin == 0;
-  p.vec_stage = p.vec_bc && p.vec_in;
-  p.use_tma = 0;
-  p.tblock = L;
-  p.nblocks = 1;
-  p.summ = nullptr;
-  p.start = nullptr;
-  p.conv_w = nullptr;
-  p.conv_b = nullptr;
+  bool done = false;
+  selscan_status_t st = prepare_fwd(shape, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, out, h_last,
+                                    false, nullptr, nullptr, s, &p, &done);
+  if (st != SELSCAN_OK || done) return st;
   bool too_big = false;
-  cudaError_t e = selscan::launch_fwd_seq_noalloc(p, shape->in_dtype, shape->out_dtype, s, &too_big);
+  cudaError_t e;
+  if (rows_path(p, shape->in_dtype)) {
+    selscan::RowsOptions o;
+    o.scratch = selscan::ScratchSource::Fixed;
+    e = selscan::launch_fwd_rows(p, shape->in_dtype, shape->out_dtype, o, s, &too_big);
+  } else {
+    e = selscan::launch_fwd_seq_noalloc(p, shape->in_dtype, shape->out_dtype, s, &too_big);
+  }
   if (e != cudaSuccess) return cuda_fail(e);
   return too_big ? SELSCAN_ERR_SCRATCH : SELSCAN_OK;
 }
@@ -489,7 +383,9 @@ int selscan_device_status(int reset) {
   int v = 0, w = 0;
   if (selscan::read_device_error(&v, reset) != cudaSuccess) return -1;
   if (selscan::read_seq_device_error(&w, reset) != cudaSuccess) return -1;
-  return v | w;
+  int x = 0;
+  if (selscan::read_rows_device_error(&x, reset) != cudaSuccess) return -1;
+  return v | w | x;
 }
 
 int selscan_abi_version(void) { return SELSCAN_ABI_VERSION; }

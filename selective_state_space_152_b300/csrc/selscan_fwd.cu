@@ -616,7 +616,12 @@ bool use_sequential(const FwdParams& p) {
   return rows < 4096 || rows >= 16384;
 }
 
+// The row-sequential kernel (selscan_rows.cu) wherever its tensor copies can stage the inputs; the
+// older kernels otherwise.  SELSCAN_KERNEL=rows|seq|chunk forces one (for tuning runs and tests).
 cudaError_t launch_fwd(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s) {
+  const char* k = getenv("SELSCAN_KERNEL");
+  if ((!k || k[0] == 'r') && rows_kernel_supports(p, in_dtype))
+    return launch_fwd_rows(p, in_dtype, out_dtype, RowsOptions{}, s, nullptr);
   if (use_sequential(p)) return launch_fwd_seq(p, in_dtype, out_dtype, s);
   if (in_dtype == SELSCAN_F32) {
     return out_dtype == SELSCAN_F32 ? dispatch_ns<float, float>(p, s) : dispatch_ns<float, __nv_bfloat16>(p, s);

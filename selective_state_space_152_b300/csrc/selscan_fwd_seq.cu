@@ -256,7 +256,6 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
   const int64_t L = p.seqlen;
   const int kslot = blockIdx.z;  // summary slot (summary pass) or time block (scan)
   const int kblk = (SUMMARY && REV) ? kslot + 1 : kslot;  // time block: steps [tbeg, tend)
-  const int first_blk = REV ? p.nblocks - 1 : 0;         // the block that starts from h0
   const int64_t tbeg = static_cast<int64_t>(kblk) * p.tblock;
   const int64_t tend = (tbeg + p.tblock) < L ? (tbeg + p.tblock) : L;
   const int64_t c_begin = tbeg / T;               // tblock is a multiple of T
@@ -313,7 +312,7 @@ __global__ void __launch_bounds__(R * 32, SELSCAN_SEQ_WARPS_PER_SM / R)
       a[k] = ok ? p.A[d * N + n] * kLog2e : 0.f;
       if (SUMMARY)
         hh[k] = 0.f;
-      else if (kblk != first_blk)
+      else if (p.nblocks > 1)  // every block's start state, the first one's copied from h0 by the carry pass
         hh[k] = ok ? p.start[(kblk * rows_total + grow) * N + n] : 0.f;
       else
         hh[k] = (ok && p.h0) ? p.h0[grow * N + n] : 0.f;
@@ -602,6 +601,9 @@ __global__ void __launch_bounds__(256) selscan_carry_kernel(const FwdParams p) {
   const int64_t d = grow % p.dim;
   const float A2 = p.A[d * N + n] * kLog2e;
   float st = p.h0 ? p.h0[grow * N + n] : 0.f;
+  // The first block in scan order starts from h0, copied into its slot: the scan pass then never reads
+  // h0, which h_last may overwrite (in-place carry) while other blocks of the same launch still run.
+  p.start[((REV ? p.nblocks - 1 : 0) * rows + grow) * N + n] = st;
 #pragma unroll 8
   for (int k = 0; k < p.nblocks - 1; k++) {
     // Forward: summary slot k is block k and feeds block k+1.  Reverse: slot nblocks-2-k is block
@@ -766,40 +768,9 @@ cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan
                                   : dispatch_seq<__nv_bfloat16, __nv_bfloat16>(p, s);
 }
 
-// ---- selscan_fwd_noalloc: the time-block scratch in a fixed device array ---------------------------
-//
-// For callers that may not allocate memory while they run.  The summaries and start states of the
-// time blocks live in this array instead of stream-ordered scratch; it is reserved on every GPU that
-// loads the library, for the life of the process.  Host code may not use the array's name as a
-// device address (in host code it names a host-side stand-in), so its device address is looked up
-// once per device with cudaGetSymbolAddress, with that device current, and passed to the kernels.
-// Calls share the array: work of calls that overlaps on the GPU races on it.
-
-constexpr size_t kNoAllocFloats = SELSCAN_NOALLOC_SCRATCH_BYTES / sizeof(float);
-static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
+// ---- selscan_fwd_noalloc on rows that the row-sequential kernel cannot stage ------------------------
 
 namespace {
-
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
-// Device address of the array on the current device (looked up on the first call per device).
-cudaError_t noalloc_scratch(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<float*>(ptr);
-  }
-  *out = g_noalloc_ptr[dev];
-  return cudaSuccess;
-}
 
 // As launch_seq_cfg, with the scratch taken from the fixed array.
 template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
@@ -843,13 +814,14 @@ cudaError_t launch_seq_noalloc_cfg(const FwdParams& p_in, cudaStream_t s, bool* 
   const int64_t N = p.dstate;
   const size_t summ_floats = static_cast<size_t>(p.nblocks - 1) * rows * (N + 1);
   const size_t start_floats = static_cast<size_t>(p.nblocks) * rows * N;
-  if (summ_floats + start_floats > kNoAllocFloats) {
+  float* ws = nullptr;
+  size_t cap_bytes = 0;
+  e = fixed_scratch(&ws, &cap_bytes);
+  if (e != cudaSuccess) return e;
+  if ((summ_floats + start_floats) * sizeof(float) > cap_bytes) {
     *too_big = true;
     return cudaSuccess;
   }
-  float* ws = nullptr;
-  e = noalloc_scratch(&ws);
-  if (e != cudaSuccess) return e;
   // Every summary entry is written by the summary pass and every start entry by the carry pass
   // before it is read, so nothing in the array needs clearing.
   p.summ = ws;

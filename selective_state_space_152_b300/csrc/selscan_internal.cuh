@@ -43,6 +43,11 @@ struct FwdParams {
   // Convolution front (selscan_fwd_conv): u = silu(conv_b + Σ_k conv_w[d,k]·x[t-3+k]); `u` then holds x.
   const float* conv_w;  // [D, 4]
   const float* conv_b;  // [D], nullable
+  // Row-sequential kernel (selscan_rows.cu): consumer warps per CTA, pipeline stages, and the output
+  // type (set by its launcher).
+  int warps;
+  int stages;
+  int out_bf16;
 };
 
 // Arguments of one selscan_step launch.
@@ -103,6 +108,28 @@ cudaError_t launch_fwd_seq_noalloc(const FwdParams& p, selscan_dtype_t in_dtype,
 // Read (and optionally clear) the device-side failure words set by a kernel's bounded wait.
 cudaError_t read_device_error(int* value, int reset);
 cudaError_t read_seq_device_error(int* value, int reset);
+cudaError_t read_rows_device_error(int* value, int reset);
+
+// Where the time-block scratch of a forward call comes from: the CUDA memory pool of the call's stream
+// (cudaMallocAsync / cudaFreeAsync), or the library's fixed device array (selscan_fwd_noalloc).
+enum class ScratchSource { Pool, Fixed };
+// Device address and size of the fixed array on the current device (looked up once per device).
+cudaError_t fixed_scratch(float** ptr, size_t* bytes);
+
+// Options of the row-sequential forward kernel (selscan_rows.cu).
+struct RowsOptions {
+  bool reverse = false;
+  bool zoh = false;
+  bool conv = false;
+  ScratchSource scratch = ScratchSource::Pool;
+};
+// True when the row-sequential kernel can run the call: every input row 16-byte aligned for tensor
+// copies (vec_stage) and sizes whose copy coordinates fit in 32 bits.
+bool rows_kernel_supports(const FwdParams& p, selscan_dtype_t in_dtype);
+// The row-sequential forward (time blocks chosen by the launcher).  With ScratchSource::Fixed it sets
+// *too_big and enqueues nothing when the time blocks need more than the fixed array holds.
+cudaError_t launch_fwd_rows(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype,
+                            const RowsOptions& o, cudaStream_t s, bool* too_big);
 
 // ---------------------------------------------------------------------------------------------
 // Device helpers
@@ -269,6 +296,9 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 }
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");

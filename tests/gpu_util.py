@@ -112,6 +112,20 @@ def sample_rows(Bsz, Dm, k, seed=0):
     return sorted(rows)
 
 
+def decode_as_forward(inp):
+    """A decode input ([T, B, D] / [T, B, N] per-step tensors) as one forward problem over its T steps:
+    u, delta, z become [B, D, T] and B, C [B, N, T]; h0 stays the start state.  T decode steps carrying
+    the state equal the forward over those T steps (an oracle pin), so the oracle can check every row of
+    a full-size decode run with its threaded forward."""
+    T = inp["steps"]
+    Bsz, Dm, _, N = inp["shape"]
+    mv = lambda a: None if a is None else np.ascontiguousarray(np.moveaxis(np.asarray(a), 0, -1))  # noqa: E731
+    return {"shape": (Bsz, Dm, T, N), "in_dtype": inp["in_dtype"], "steps": 0,
+            "u": mv(inp["u"]), "delta": mv(inp["delta"]), "z": mv(inp.get("z")), "B": mv(inp["B"]),
+            "C": mv(inp["C"]), "A": inp["A"], "D": inp.get("D"), "delta_bias": inp.get("delta_bias"),
+            "h0": inp.get("h0")}
+
+
 def decode_as_sequences(inp, rows):
     """Rearrange a decode input ([T, B, D] / [T, B, N]) into forward problems over its steps.
 

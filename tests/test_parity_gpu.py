@@ -5,31 +5,32 @@ Tolerances (written here, derived from the required accuracy of the scan):
   bf16 inputs, fp32 state: |out - ref| <= 2e-3 + 2e-3·|ref|
   h_last:                 |h - ref| <= 1e-4 · max_n |ref| of the channel (relative, in the max norm
                           of each channel's state vector)
-Full-size workloads are compared on sampled rows that the oracle computes
-one by one; small shapes (ragged L, odd dstate, channel counts that do not
-fill a CTA) are compared in full.
+Every case is compared in full, every element of every output, including the
+full-size workloads in the launch configuration that bench.py times (the
+oracle runs on all host cores) and all 64 steps of the decode workload.
 """
 import numpy as np
 import pytest
 
 import oracle
 import seeded_inputs as si
-from gpu_util import (check_h, check_out, decode_as_sequences, gpu_fwd, gpu_fwd_conv, gpu_fwd_ex, sample_rows,
+from gpu_util import (check_h, check_out, decode_as_forward, gpu_fwd, gpu_fwd_conv, gpu_fwd_ex, sample_rows,
                       to_dev)
 
 pytestmark = pytest.mark.gpu
 
-# Both forward kernels: "seq" walks each row sequentially (rows spread over lanes), "chunk" splits
-# each row's sequence over lanes and joins them with a scan.  The library picks by shape; the tests
-# force each one through the SELSCAN_KERNEL override.  "chunk_direct" is the chunked kernel with its
-# tensor-copy staging turned off (SELSCAN_STAGING=0), so that its direct-load path is also covered
-# on aligned inputs.
-KERNELS = ["seq", "chunk", "chunk_direct"]
+# The forward kernels: "rows" is the row-sequential kernel with the warp-specialised copy pipeline
+# (the library's choice wherever every input row is 16-byte aligned; elsewhere these cases fall back to
+# "seq"); "seq" is the older sequential kernel (rows spread over lanes, in-CTA staging), "chunk" splits
+# each row's sequence over lanes and joins them with a scan.  The tests force each one through the
+# SELSCAN_KERNEL override.  "chunk_direct" is the chunked kernel with its tensor-copy staging turned off
+# (SELSCAN_STAGING=0), so that its direct-load path is also covered on aligned inputs.
+KERNELS = ["rows", "seq", "chunk", "chunk_direct"]
 
 
 @pytest.fixture(params=KERNELS)
 def kernel(request, monkeypatch):
-    monkeypatch.setenv("SELSCAN_KERNEL", "seq" if request.param == "seq" else "chunk")
+    monkeypatch.setenv("SELSCAN_KERNEL", {"rows": "rows", "seq": "seq"}.get(request.param, "chunk"))
     if request.param == "chunk_direct":
         monkeypatch.setenv("SELSCAN_STAGING", "0")
     else:
@@ -113,21 +114,61 @@ def test_chunked_staged_shapes(case, lanes, monkeypatch):
     check_h(hl, href)
 
 
-# Time blocks of the sequential kernel: the sequence is cut into blocks joined by a summary pass
-# (each block's zero-start end state and ΣΔ) and a carry pass.  Forced block counts on ragged
-# lengths, with and without h0, softplus on and off, fp32 and bf16.
+# The row-sequential kernel's geometry, forced: 4 or 8 states per lane (4 or 2 lanes per row), 1, 3
+# or 15 consumer warps per CTA, 2 or 4 pipeline stages.  Lengths are whole 16-byte rows (so the kernel
+# can stage them) but ragged against its 32-step chunks; channel counts leave the last CTA's rows partly
+# past `dim`; dstate below the 4/8/16-state tile; both dtypes; with and without the gate.
+ROWS_CASES = [
+    (101, 2, 40, 1000, 16, "bf16", True),
+    (102, 3, 17, 264, 12, "bf16", True),
+    (103, 1, 8, 4096, 16, "bf16", False),
+    (104, 2, 24, 300, 5, "f32", True),
+    (105, 1, 33, 772, 16, "f32", True),
+    (106, 2, 16, 64, 3, "bf16", True),
+    (107, 1, 130, 96, 8, "f32", False),
+    (108, 2, 70, 200, 4, "bf16", True),
+]
+ROWS_GEOM = [("4", "1", "2"), ("4", "3", "4"), ("8", "15", "3"), ("8", "2", "2"), ("4", "15", "2")]
+
+
+@pytest.mark.parametrize("geom", ROWS_GEOM, ids=[f"spl{g[0]}_w{g[1]}_s{g[2]}" for g in ROWS_GEOM])
+@pytest.mark.parametrize("case", ROWS_CASES, ids=[f"s{c[0]}_B{c[1]}D{c[2]}L{c[3]}N{c[4]}_{c[5]}" for c in ROWS_CASES])
+def test_rows_kernel_geometry(case, geom, monkeypatch):
+    monkeypatch.setenv("SELSCAN_KERNEL", "rows")
+    monkeypatch.setenv("SELSCAN_ROWS_SPL", geom[0])
+    monkeypatch.setenv("SELSCAN_ROWS_WARPS", geom[1])
+    monkeypatch.setenv("SELSCAN_ROWS_STAGES", geom[2])
+    seed, Bsz, Dm, L, N, dt, hz = case
+    inp = si.random_case(seed, Bsz, Dm, L, N, in_dtype=dt, has_z=hz)
+    ref, href = oracle.selscan_fwd(inp)
+    got, hl = gpu_fwd(inp)
+    check_out(got, ref, dt)
+    check_h(hl, href)
+    got16, _ = gpu_fwd(inp, out_dtype="bf16", h_last=False)
+    check_out(got16, ref, dt, what="bf16 out", extra_rel=2.0 ** -8)
+
+
+# Time blocks: the sequence is cut into blocks joined by a summary pass (each block's zero-start end
+# state and ΣΔ) and a carry pass.  Forced block counts on ragged lengths, with and without h0, softplus
+# on and off, fp32 and bf16, for the row-sequential kernel (lengths of whole 16-byte rows) and the older
+# sequential kernel.
 TBLOCKED = [
     (41, 2, 5, 1500, 16, "bf16", True, True),
     (42, 1, 3, 2049, 4, "f32", True, False),
     (43, 3, 4, 1100, 12, "f32", False, True),
     (44, 1, 40, 4096, 16, "bf16", True, True),
+    (45, 2, 5, 1504, 16, "bf16", True, True),
+    (46, 1, 3, 2048, 4, "f32", True, False),
+    (47, 3, 4, 1104, 12, "f32", False, True),
+    (48, 1, 20, 1000, 8, "bf16", True, True),
 ]
 
 
+@pytest.mark.parametrize("kern", ["rows", "seq"])
 @pytest.mark.parametrize("nblocks", ["2", "3", "7"])
 @pytest.mark.parametrize("case", TBLOCKED, ids=[f"s{c[0]}_B{c[1]}D{c[2]}L{c[3]}N{c[4]}_{c[5]}" for c in TBLOCKED])
-def test_time_blocked_sequential(case, nblocks, monkeypatch):
-    monkeypatch.setenv("SELSCAN_KERNEL", "seq")
+def test_time_blocked_sequential(case, nblocks, kern, monkeypatch):
+    monkeypatch.setenv("SELSCAN_KERNEL", kern)
     monkeypatch.setenv("SELSCAN_TBLOCKS", nblocks)
     seed, Bsz, Dm, L, N, dt, hh, sp = case
     inp = si.random_case(seed, Bsz, Dm, L, N, in_dtype=dt, has_h0=hh)
@@ -232,15 +273,15 @@ def test_fwd_conv_long_sequence_sampled():
 
 
 @pytest.mark.parametrize("name", ["mamba130m_layer", "long_seq_65k", "width_2p8b"])
-def test_workload_sampled_rows(name):
+def test_workload_full(name):
+    """Every element of the full-size workload, in the launch configuration the bench times, against
+    the oracle on all host cores."""
     w = si.WORKLOADS[name]
     inp = si.make_inputs(w)
-    Bsz, Dm, L, N = inp["shape"]
     got, hl = gpu_fwd(inp)
-    rows = sample_rows(Bsz, Dm, 12 if L > 10000 else 48, seed=len(name))
-    ref, href = oracle.selscan_fwd(inp, rows=rows)
-    check_out(got.reshape(Bsz * Dm, L)[rows], ref, w.in_dtype, what=f"{name} out")
-    check_h(hl.reshape(Bsz * Dm, N)[rows], href, what=f"{name} h_last")
+    ref, href = oracle.selscan_fwd(inp)
+    check_out(got, ref, w.in_dtype, what=f"{name} out")
+    check_h(hl, href, what=f"{name} h_last")
 
 
 def test_bf16_output(kernel):
@@ -272,31 +313,55 @@ def test_carry_across_calls(kernel):
     check_h(h.cpu().numpy().astype(np.float64), href, what="chunked-call h_last")
 
 
-def test_decode_step_workload_sampled():
+@pytest.mark.parametrize("kern", ["rows", "seq"])
+@pytest.mark.parametrize("reverse", [False, True])
+def test_inplace_carry_with_time_blocks(kern, reverse, monkeypatch):
+    """h_last aliasing h0 (the in-place carry the header allows) while the sequence runs in time blocks:
+    the first block's start state must be read before the last block's end state overwrites it."""
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    monkeypatch.setenv("SELSCAN_KERNEL", kern)
+    monkeypatch.setenv("SELSCAN_TBLOCKS", "5")
+    inp = si.random_case(121, 2, 40, 2048, 16, in_dtype="bf16")
+    ref, href = oracle.selscan_fwd(inp, reverse=reverse)
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    h = t["h0"].clone()
+    out, _ = ss.selscan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                               delta_bias=t["delta_bias"], h0=h, h_last=h, reverse=reverse)
+    torch.cuda.synchronize()
+    check_out(out.cpu().numpy().astype(np.float64), ref, "bf16", what="in-place carry out")
+    check_h(h.cpu().numpy().astype(np.float64), href, what="in-place carry h_last")
+
+
+def test_decode_step_workload_full():
+    """The decode workload as stated: all 64 steps over the full 256 x 5120 batch, carrying the state.
+    Every output of every step and the final state are compared with the oracle.  T decode steps
+    carrying the state equal the forward over those T steps (an oracle pin), so the oracle runs the
+    whole decode as one threaded forward over [B, D, T]."""
     import torch
 
     import selective_state_space_152_b300 as ss
 
     w = si.WORKLOADS["decode_step"]
-    inp = si.make_inputs(w, steps=16)  # full batch and width, 16 of the 64 steps
+    inp = si.make_inputs(w)
     Bsz, Dm, _, N = inp["shape"]
     T = inp["steps"]
+    assert T == 64
     dev = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
     state = dev["h0"].clone()
-    outs = []
+    out = torch.empty((T, Bsz, Dm), device="cuda", dtype=torch.float32)
     for s in range(T):
-        o = ss.selscan_step(dev["u"][s], dev["delta"][s], dev["A"], dev["B"][s], dev["C"][s], state, D=dev["D"],
-                            z=dev["z"][s], delta_bias=dev["delta_bias"])
-        outs.append(o)
+        ss.selscan_step(dev["u"][s], dev["delta"][s], dev["A"], dev["B"][s], dev["C"][s], state, D=dev["D"],
+                        z=dev["z"][s], delta_bias=dev["delta_bias"], out=out[s])
     torch.cuda.synchronize()
-    got = torch.stack(outs).cpu().numpy().astype(np.float64)  # [T, B, D]
+    got = out.cpu().numpy().astype(np.float64)  # [T, B, D]
     hs = state.cpu().numpy().astype(np.float64)
-    rows = sample_rows(Bsz, Dm, 64, seed=5)
-    for r, case in zip(rows, decode_as_sequences(inp, rows)):
-        b, d = divmod(r, Dm)
-        ref, href = oracle.selscan_fwd(case, nthreads=1)
-        check_out(got[:, b, d], ref[0, 0], "bf16", what=f"decode row {r}")
-        check_h(hs[b, d], href[0, 0], what=f"decode state row {r}")
+    seq = decode_as_forward(inp)
+    ref, href = oracle.selscan_fwd(seq)  # [B, D, T], [B, D, N]
+    check_out(np.moveaxis(got, 0, -1), ref, "bf16", what="decode out (all steps)")
+    check_h(hs, href, what="decode state after 64 steps")
 
 
 def test_step_small_fp32_odd_dstate():
