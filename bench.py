@@ -19,6 +19,10 @@ over three streams: copies in, scan, copies out); ``cpu_baseline`` = the fp64 or
 on the host cores on a bounded row sample; ``decode`` = the recurrent decode
 step workload (secondary).  Under torchrun (N > 1) every rank runs its own
 shard of an N-times-larger batch (weak scaling, no data-path collective).
+``sweep`` times the other forward workloads of the same family (the 65536-step
+sequence and the 2.8B-width layer) the same way, each with its own roofline;
+``unit_rates`` are the special-function and FMA rates measured on the GPU by the
+library's own probe (selscan_probe_rate), from which the rooflines are derived.
 """
 from __future__ import annotations
 
@@ -42,8 +46,9 @@ import seeded_inputs as si  # noqa: E402
 METRIC = "selective-scan elems(B·D·L)/s and HBM GB/s at 1 B300; fraction of roofline"
 DEFAULT_WORKLOAD = "mamba130m_layer"
 L2_FLUSH_BYTES = 256 << 20
-EX2_PER_CLK_PER_SM = 32  # measured on B300: ex2.approx.ftz.f32 issues 32 results / clock / SM
-FP32_PER_CLK_PER_SM = 128  # FFMA lanes per SM
+# Results per clock per SM of the units the forward needs, used only when the probe cannot run (no GPU):
+# the values selscan_probe_rate measured on B300 (ex2 32; lg2 and rcp at half that rate; fp32 FMA 128).
+FALLBACK_RATES = {"ex2": 32.0, "lg2": 16.0, "rcp": 16.0, "ffma2": 128.0}
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_SM_MHZ = 2032.0
 
@@ -63,13 +68,14 @@ def measured_peaks(path=os.path.join(ROOT, "MEASURED_PEAKS.json")):
 
 
 def fwd_work(batch, dim, seqlen, dstate, in_bytes=2, out_bytes=4, h0=False, h_last=True):
-    """Algorithmic work of one selscan_fwd: elements, bytes, MUFU ops and FP32 ops.
+    """Algorithmic work of one selscan_fwd: elements, bytes, special-function ops and FP32 ops.
 
     Bytes: u, δ, z read once and out written once per element; B, C read once
     per (b, n, t) — not per channel; A, D, Δ_bias once; h0 / h_last once.
-    MUFU: N exponentials for Ā plus 4 for softplus (exp, log) and the gate
-    (exp, reciprocal) per element.  FP32: 4 per (element, state) — Δ·A, Δu·B,
-    the state FMA, the C·h FMA — plus 8 per element.
+    Special functions per element: N exponentials for Ā, an exponential and a
+    logarithm for softplus, an exponential and a reciprocal for the gate
+    ("ex2": N + 2, "lg2": 1, "rcp": 1).  FP32: 4 per (element, state) — Δ·A,
+    Δu·B, the state FMA, the C·h FMA — plus 8 per element.
     """
     elems = batch * dim * seqlen
     nbytes = elems * (3 * in_bytes + out_bytes) + 2 * batch * dstate * seqlen * in_bytes + dim * dstate * 4 + 2 * dim * 4
@@ -77,7 +83,8 @@ def fwd_work(batch, dim, seqlen, dstate, in_bytes=2, out_bytes=4, h0=False, h_la
         nbytes += batch * dim * dstate * 4
     if h_last:
         nbytes += batch * dim * dstate * 4
-    return {"elements": elems, "bytes": nbytes, "mufu": elems * (dstate + 4), "fp32": elems * (4 * dstate + 8)}
+    return {"elements": elems, "bytes": nbytes, "mufu": elems * (dstate + 4),
+            "sfu": {"ex2": elems * (dstate + 2), "lg2": elems, "rcp": elems}, "fp32": elems * (4 * dstate + 8)}
 
 
 def step_work(batch, dim, dstate, in_bytes=2, out_bytes=4):
@@ -88,27 +95,36 @@ def step_work(batch, dim, dstate, in_bytes=2, out_bytes=4):
             + dim * dstate * 4 + 2 * dim * 4}
 
 
-def roofline_times(work, sms, hbm_gbs, sm_mhz):
-    """Seconds each resource needs at its peak: HBM bytes, MUFU ops, FP32 ops."""
+def mufu_slots(work, rates):
+    """Special-function work in ex2-equivalent issue slots: each unit's ops scaled by ex2's rate over its own."""
+    sfu = work.get("sfu") or {"ex2": work["mufu"]}
+    return sum(n * rates["ex2"] / rates[u] for u, n in sfu.items())
+
+
+def roofline_times(work, sms, hbm_gbs, sm_mhz, rates=None):
+    """Seconds each resource needs at its peak: HBM bytes, special-function ops (each unit at its measured
+    rate), FP32 ops."""
+    rates = rates or FALLBACK_RATES
     f = sm_mhz * 1e6
-    return {"hbm": work["bytes"] / (hbm_gbs * 1e9), "mufu": work["mufu"] / (sms * EX2_PER_CLK_PER_SM * f),
-            "fp32": work["fp32"] / (sms * FP32_PER_CLK_PER_SM * f)}
+    return {"hbm": work["bytes"] / (hbm_gbs * 1e9), "mufu": mufu_slots(work, rates) / (sms * rates["ex2"] * f),
+            "fp32": work["fp32"] / (sms * rates["ffma2"] * f)}
 
 
-def roofline_entry(work, t_kernel, sms, hbm_gbs, sm_mhz, traffic=None):
+def roofline_entry(work, t_kernel, sms, hbm_gbs, sm_mhz, traffic=None, rates=None):
     """The roofline object for a forward kernel that took t_kernel seconds per launch."""
-    t = roofline_times(work, sms, hbm_gbs, sm_mhz)
+    rates = rates or FALLBACK_RATES
+    t = roofline_times(work, sms, hbm_gbs, sm_mhz, rates)
     bound = max(t, key=t.get)
     if bound == "hbm":
         achieved, peak, unit = work["bytes"] / t_kernel / 1e9, hbm_gbs, "GB/s"
         kind = "hbm"
     elif bound == "mufu":
-        achieved = work["mufu"] / t_kernel / 1e12
-        peak = sms * EX2_PER_CLK_PER_SM * sm_mhz * 1e6 / 1e12
+        achieved = mufu_slots(work, rates) / t_kernel / 1e12
+        peak = sms * rates["ex2"] * sm_mhz * 1e6 / 1e12
         unit, kind = "TFLOP/s", "alu"
     else:
         achieved = work["fp32"] / t_kernel / 1e12
-        peak = sms * FP32_PER_CLK_PER_SM * sm_mhz * 1e6 / 1e12
+        peak = sms * rates["ffma2"] * sm_mhz * 1e6 / 1e12
         unit, kind = "TFLOP/s", "alu"
     return {"bound": kind, "resource": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "traffic": traffic,
@@ -140,7 +156,7 @@ def max_over_ranks(seconds, dist, device):
 
 
 # The sources each kernel is built from (its own file and the shared device helpers).
-KERNEL_SOURCES = {"selscan_fwd": ("selscan_fwd.cu", "selscan_fwd_seq.cu", "selscan_internal.cuh"),
+KERNEL_SOURCES = {"selscan_fwd": ("selscan_rows.cu", "selscan_fwd.cu", "selscan_fwd_seq.cu", "selscan_internal.cuh"),
                   "selscan_step": ("selscan_step.cu", "selscan_internal.cuh")}
 
 
@@ -169,20 +185,33 @@ def recorded_traffic(kernel, workload, path=os.path.join(ROOT, "profiles", "ncu_
 
 
 class ClockSampler:
-    """Polls SM clock and clock-event reasons through NVML while the timed region runs."""
+    """Samples the SM clock and the clock-event reasons while the benchmark runs.
+
+    Sampling starts before the warm-up (``start``, which waits for the first sample: nvidia-smi takes
+    a moment to begin) and stops after the run; ``mark_begin`` / ``mark_end`` bracket the timed region
+    and ``report`` keeps the samples taken inside it.  NVML is used where importable, else nvidia-smi
+    polling.
+    """
 
     REASONS = {"hw_slowdown": "nvmlClocksEventReasonHwSlowdown",
                "hw_thermal_slowdown": "nvmlClocksEventReasonHwThermalSlowdown",
                "sw_thermal_slowdown": "nvmlClocksEventReasonSwThermalSlowdown",
                "sw_power_cap": "nvmlClocksEventReasonSwPowerCap",
                "hw_power_brake": "nvmlClocksEventReasonHwPowerBrakeSlowdown"}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+    SMI_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, device_index, period_s=0.005, smi_id=None):
-        self.samples, self.reasons, self.max_mhz, self.error = [], set(), None, None
+    def __init__(self, device_index, period_s=0.02, smi_id=None):
+        self.samples = []  # (time, sm MHz, set of active reasons)
+        self.max_mhz, self.error = None, None
         self.smi_id = smi_id if smi_id is not None else str(device_index)
         self.period = period_s
+        self.begin = self.end = None
         self._stop = threading.Event()
         self._t = None
+        self._proc = None
         try:
             import pynvml
 
@@ -193,65 +222,78 @@ class ClockSampler:
         except Exception as e:  # noqa: BLE001 - fall back to nvidia-smi polling
             self.nv = None
             self.error = f"{type(e).__name__}: {e}"
-        self.device_index = device_index
-        self._proc = None
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
                 r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                for name, const in self.REASONS.items():
-                    if r & getattr(nv, const, 0):
-                        self.reasons.add(name)
+                reasons = {name for name, const in self.REASONS.items() if r & getattr(nv, const, 0)}
+                self.samples.append((time.perf_counter(), float(mhz), reasons))
             except Exception:  # noqa: BLE001
                 pass
             time.sleep(self.period)
 
-    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-                  "clocks_event_reasons.sw_power_cap")
+    def _run_smi(self):
+        for line in self._proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                mhz = float(f[0])
+                self.max_mhz = float(f[1])
+            except ValueError:
+                continue
+            reasons = {n for n, v in zip(self.SMI_NAMES, f[2:6]) if v.lower() == "active"}
+            self.samples.append((time.perf_counter(), mhz, reasons))
 
-    def __enter__(self):
+    def start(self, wait_s=5.0):
         if self.nv is not None:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
         else:
             import subprocess
 
             try:
                 self._proc = subprocess.Popen(
-                    ["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
-                     "-i", self.smi_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                    ["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", str(max(20, int(self.period * 1000))), "-i", self.smi_id],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
             except OSError as e:
                 self.error = (self.error or "") + f"; nvidia-smi: {e}"
+                return self
+            self._t = threading.Thread(target=self._run_smi, daemon=True)
+        self._t.start()
+        t0 = time.perf_counter()
+        while not self.samples and time.perf_counter() - t0 < wait_s:
+            time.sleep(0.01)
         return self
 
-    def __exit__(self, *exc):
+    def mark_begin(self):
+        self.begin = time.perf_counter()
+
+    def mark_end(self):
+        self.end = time.perf_counter()
+
+    def stop(self):
         self._stop.set()
-        if self._t:
-            self._t.join()
         if self._proc is not None:
             self._proc.terminate()
-            out, _ = self._proc.communicate(timeout=10)
-            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-            for line in out.splitlines():
-                f = [x.strip() for x in line.split(",")]
-                if len(f) < 6:
-                    continue
-                try:
-                    self.samples.append(float(f[0]))
-                    self.max_mhz = float(f[1])
-                except ValueError:
-                    continue
-                for name, v in zip(names, f[2:6]):
-                    if v.lower() == "active":
-                        self.reasons.add(name)
+            try:
+                self._proc.wait(timeout=10)
+            except Exception:  # noqa: BLE001
+                self._proc.kill()
+        if self._t is not None:
+            self._t.join(timeout=10)
 
     def report(self):
-        r = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
-             "reasons": sorted(self.reasons), "samples": len(self.samples),
+        lo = self.begin if self.begin is not None else -float("inf")
+        hi = self.end if self.end is not None else float("inf")
+        inside = [(mhz, rs) for t, mhz, rs in self.samples if lo <= t <= hi]
+        reasons = set().union(*[rs for _, rs in inside]) if inside else set()
+        r = {"sm_mhz": statistics.median([m for m, _ in inside]) if inside else None, "sm_max_mhz": self.max_mhz,
+             "reasons": sorted(reasons), "samples": len(inside), "samples_total": len(self.samples),
+             "timed_region_s": (hi - lo) if self.begin is not None and self.end is not None else None,
              "source": "nvml" if self.nv is not None else "nvidia-smi"}
         if self.error:
             r["nvml_error"] = self.error
@@ -280,6 +322,42 @@ def _pinned(torch, a):
     return torch.from_numpy(a).pin_memory()
 
 
+def workload_config(w, batch, seqlen):
+    """The `config` object of a bench line (both arms print the same one)."""
+    return {"workload": w.name, "batch": batch, "dim": w.dim, "seqlen": seqlen, "dstate": w.dstate,
+            "in_dtype": w.in_dtype, "out_dtype": "f32", "state": "f32",
+            "l2": "flushed (256 MiB write) before every timed step, outside its events"}
+
+
+def measure_rates(ss):
+    """The special-function and FMA rates of this GPU (results per clock per SM) from the library's probe."""
+    try:
+        return {u: ss.selscan_probe_rate(u) for u in ("ex2", "lg2", "rcp", "ffma2")}, "measured (selscan_probe_rate)"
+    except Exception as e:  # noqa: BLE001
+        return dict(FALLBACK_RATES), f"fallback ({type(e).__name__})"
+
+
+def time_forward(torch, fwd, stream, flush, steps):
+    """CUDA-event time of each of `steps` calls, each after an L2 flush outside its events."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        fwd()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) / 1e3 for a, b in zip(starts, ends)]
+
+
+def forward_tensors(torch, inp, w, device):
+    t = {k: _dev(torch, inp.get(k), device) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    Bsz, Dm, L, N = inp["shape"]
+    out = torch.empty((Bsz, Dm, L), device=device, dtype=torch.float32)
+    h_last = torch.empty((Bsz, Dm, N), device=device, dtype=torch.float32) if w.returns_h_last else None
+    return t, out, h_last
+
+
 def run_ours(args, rank, world, local_rank, dist):
     import torch
 
@@ -293,12 +371,10 @@ def run_ours(args, rank, world, local_rank, dist):
     lo, hi = shard_batch(w.batch * world, rank, world)
     inp = si.make_inputs(w, seed=si.BASE_SEED + si.WORKLOAD_ORDER.index(w.name) + 1000 * rank, batch=hi - lo)
     Bsz, Dm, L, N = inp["shape"]
-    names = ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")
-    t = {k: _dev(torch, inp.get(k), device) for k in names}
-    out = torch.empty((Bsz, Dm, L), device=device, dtype=torch.float32)
-    h_last = torch.empty((Bsz, Dm, N), device=device, dtype=torch.float32) if w.returns_h_last else None
+    t, out, h_last = forward_tensors(torch, inp, w, device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=device, dtype=torch.float32)
     stream = torch.cuda.current_stream()
+    rates, rates_src = measure_rates(ss)
 
     def fwd():
         ss.selscan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"], delta_bias=t["delta_bias"],
@@ -308,28 +384,23 @@ def run_ours(args, rank, world, local_rank, dist):
         if dist is not None:
             dist.barrier()
 
+    props = torch.cuda.get_device_properties(device)
+    smi_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local_rank)
+    clk = ClockSampler(local_rank, smi_id=smi_id).start()
     for _ in range(args.warmup):
         flush.zero_()
         fwd()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches_per_call = ss.selscan_last_launch_count()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
-    props = torch.cuda.get_device_properties(device)
-    smi_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local_rank)
-    with ClockSampler(local_rank, smi_id=smi_id) as clk:
-        wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            fwd()
-            ends[i].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
+    clk.mark_begin()
+    wall0 = time.perf_counter()
+    step_s = time_forward(torch, fwd, stream, flush, args.steps)
+    wall = time.perf_counter() - wall0
+    clk.mark_end()
     barrier()
     torch.cuda.synchronize()
-    step_s = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
     t_sum = sum(step_s)
     t_max = max_over_ranks(t_sum, dist, device)
     elems_rank = Bsz * Dm * L * args.steps
@@ -337,35 +408,75 @@ def run_ours(args, rank, world, local_rank, dist):
 
     work = fwd_work(Bsz, Dm, L, N, in_bytes=2 if w.in_dtype == "bf16" else 4, out_bytes=4,
                     h0=inp.get("h0") is not None, h_last=h_last is not None)
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    sms = props.multi_processor_count
     hbm_gbs, sm_mhz, peak_src = measured_peaks()
     t_kernel = t_sum / args.steps
-    roof = roofline_entry(work, t_kernel, sms, hbm_gbs, sm_mhz,
+    roof = roofline_entry(work, t_kernel, sms, hbm_gbs, sm_mhz, rates=rates,
                           traffic=recorded_traffic("selscan_fwd", args.workload))
-    roof["peak_source"] = f"{peak_src} (HBM {hbm_gbs} GB/s; SM {sm_mhz} MHz x {sms} SMs)"
+    roof["peak_source"] = (f"HBM {hbm_gbs} GB/s ({peak_src} copy bandwidth); special-function and FMA rates "
+                           f"{rates_src}; SM {sm_mhz} MHz x {sms} SMs")
 
     result = {
         "metric": METRIC, "value": value, "unit": "elems/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "batch": Bsz * world, "dim": Dm, "seqlen": L, "dstate": N,
-                   "in_dtype": w.in_dtype, "out_dtype": "f32", "state": "f32",
-                   "l2": "flushed (256 MiB write) before every timed step, outside its events"},
+        "config": workload_config(w, Bsz * world, L),
         "hbm_gbs": work["bytes"] * world * args.steps / t_max / 1e9,
         "roofline": roof,
-        "gpu_launches": args.steps,
-        "clocks": clk.report(),
+        "gpu_launches": args.steps * launches_per_call,
+        "unit_rates": dict(rates, source=rates_src, unit="results per clock per SM"),
         "wall_s_timed_region": wall,
     }
+    if rank == 0 and world == 1 and not args.no_sweep:
+        result["sweep"] = run_sweep(args, torch, ss, device, stream, flush, sms, hbm_gbs, sm_mhz, rates)
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world)
     if rank == 0 and world == 1 and not args.no_decode:
         result["decode"] = run_decode(args, torch, ss, device, stream, flush, sms, hbm_gbs)
     if rank == 0 and world == 1 and not args.no_options:
-        result["options"] = run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz)
+        result["options"] = run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz, rates)
+    clk.stop()
+    result["clocks"] = clk.report()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, w, budget_cpu_s=args.cpu_budget)
     return result
+
+
+SWEEP_WORKLOADS = ("mamba130m_layer", "long_seq_65k", "width_2p8b")
+
+
+def run_sweep(args, torch, ss, device, stream, flush, sms, hbm_gbs, sm_mhz, rates):
+    """Every forward workload of the family timed like the headline (CUDA events per call, L2 flushed
+    before each), each against its own roofline."""
+    res = {}
+    for name in SWEEP_WORKLOADS:
+        w = si.WORKLOADS[name]
+        inp = si.make_inputs(w)
+        Bsz, Dm, L, N = inp["shape"]
+        t, out, h_last = forward_tensors(torch, inp, w, device)
+
+        def fwd():
+            ss.selscan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                           delta_bias=t["delta_bias"], delta_softplus=True, h0=t["h0"], out=out, h_last=h_last,
+                           stream=stream)
+
+        for _ in range(3):
+            flush.zero_()
+            fwd()
+        launches = ss.selscan_last_launch_count()
+        steps = max(5, args.sweep_steps)
+        secs = time_forward(torch, fwd, stream, flush, steps)
+        t_call = statistics.median(secs)
+        work = fwd_work(Bsz, Dm, L, N, in_bytes=2 if w.in_dtype == "bf16" else 4, out_bytes=4,
+                        h0=inp.get("h0") is not None, h_last=h_last is not None)
+        roof = roofline_entry(work, t_call, sms, hbm_gbs, sm_mhz, rates=rates,
+                              traffic=recorded_traffic("selscan_fwd", name))
+        res[name] = {"config": workload_config(w, Bsz, L), "steps": steps, "us_per_call": t_call * 1e6,
+                     "us_per_call_min": min(secs) * 1e6, "elems_per_s": work["elements"] / t_call,
+                     "hbm_gbs": work["bytes"] / t_call / 1e9, "roofline": roof, "launches_per_call": launches}
+        del t, out, h_last
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world):
@@ -437,7 +548,7 @@ def run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world):
             "gpu_launches": steps, "pipelined": "h2d / scan / d2h on three streams, two buffer sets"}
 
 
-def run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz, steps=50):
+def run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz, rates, steps=50):
     """Secondary: the options on the same workload (selscan_fwd_ex's reverse scan and exact
     zero-order-hold input matrix; selscan_fwd_conv's conv1d + SiLU front), each call timed after an
     L2 flush, against the same roofline."""
@@ -468,7 +579,7 @@ def run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm
             e1.record(stream)
         torch.cuda.synchronize()
         secs = sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3 / steps
-        roof = roofline_entry(work, secs, sms, hbm_gbs, sm_mhz)
+        roof = roofline_entry(work, secs, sms, hbm_gbs, sm_mhz, rates=rates)
         res[name] = {"us_per_call": secs * 1e6, "elems_per_s": work["elements"] / secs,
                      "roofline_frac": roof["frac"], "gpu_launches": steps}
     return res
@@ -566,8 +677,7 @@ def run_reference(args):
     return {"metric": METRIC, "value": value, "unit": "elems/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": args.workload, "batch": Bsz, "dim": Dm, "seqlen": L, "dstate": N,
-                       "in_dtype": w.in_dtype, "sample_rows_per_step": nrows},
+            "config": workload_config(w, Bsz, L),
             "cpu_baseline": {"value": value, "unit": "elems/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "elems/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -587,6 +697,8 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-options", action="store_true", help="skip the reverse / zero-order-hold timings")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the other forward workloads")
+    ap.add_argument("--sweep-steps", type=int, default=50)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -29,12 +29,17 @@
  * Conventions for every entry point:
  *  - All tensor arguments are DEVICE pointers (cudaMalloc'd, or pinned host
  *    memory mapped into the device address space) to contiguous row-major
- *    arrays, last index fastest.  The caller owns every buffer.  The library
- *    keeps no state between calls; selscan_fwd takes stream-ordered scratch
- *    (cudaMallocAsync / cudaFreeAsync on `stream`) for the time blocks of
- *    problems with few rows, and runs them in one pass instead if that
- *    allocation fails (see selscan_fwd_noalloc for a variant that allocates
- *    nothing).
+ *    arrays, last index fastest.  The caller owns every buffer.
+ *  - Scratch: selscan_fwd, selscan_fwd_ex and selscan_fwd_conv take stream-
+ *    ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`) for the
+ *    time blocks of problems with few rows (a few MB: block summaries and
+ *    start states); if the memory pool cannot supply it the call returns
+ *    SELSCAN_ERR_CUDA with cudaErrorMemoryAllocation and enqueues nothing
+ *    else.  selscan_fwd_noalloc allocates nothing.
+ *  - State kept between calls: cached device attributes and driver entry
+ *    points; per host thread, the last CUDA error and launch count; per
+ *    device, one word that a kernel sets when a bounded wait gives up
+ *    (selscan_device_status) and selscan_fwd_noalloc's fixed scratch array.
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream).  A return of SELSCAN_OK means the work was
  *    enqueued; faults during execution surface at the caller's next
@@ -50,7 +55,9 @@
  *  - h_last may alias h0 (in-place carry).  No other output may overlap an
  *    input (SELSCAN_ERR_ALIAS).
  *  - Thread safety: calls from several host threads are safe; calls on the
- *    same stream run in order.
+ *    same stream run in order.  The one exception is selscan_fwd_noalloc:
+ *    its calls share one scratch array, so calls whose work overlaps on the
+ *    GPU race (see below).
  */
 #ifndef SELSCAN_H_
 #define SELSCAN_H_
@@ -216,6 +223,17 @@ int selscan_device_status(int reset);
 
 /* SELSCAN_ABI_VERSION of the library that is loaded. */
 int selscan_abi_version(void);
+
+/*
+ * The number of kernels that the last selscan_fwd, selscan_fwd_ex, selscan_fwd_conv,
+ * selscan_fwd_noalloc or selscan_step call on this host thread enqueued: 1 for a
+ * forward run in one pass or a decode step, 3 for a forward run in time blocks (the
+ * summary pass, the carry pass and the scan), 0 when the call enqueued no kernel (an
+ * argument error, no rows, or an empty sequence, whose state is passed on by a copy).
+ * The pages have no counterpart; it lets a caller (or a benchmark) account for the
+ * launches of its timed region.
+ */
+int selscan_last_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,8 @@ STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SE
           4: "SELSCAN_ERR_UNSUPPORTED", 5: "SELSCAN_ERR_CUDA", 6: "SELSCAN_ERR_POINTER", 7: "SELSCAN_ERR_ALIAS",
           8: "SELSCAN_ERR_SCRATCH"}
 EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
-            "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_probe_rate")
+            "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_probe_rate",
+            "selscan_last_launch_count")
 # Units of selscan_probe_rate (include/selscan_probe.h).
 PROBE_UNITS = {"ex2": 0, "lg2": 1, "rcp": 2, "tanh": 3, "ffma": 4, "ffma2": 5}
 SELSCAN_FLAG_REVERSE, SELSCAN_FLAG_ZOH = 1, 2
@@ -74,6 +75,8 @@ def load_library(path: Optional[str] = None):
     lib.selscan_device_status.restype = i32
     lib.selscan_abi_version.argtypes = []
     lib.selscan_abi_version.restype = i32
+    lib.selscan_last_launch_count.argtypes = []
+    lib.selscan_last_launch_count.restype = i32
     lib.selscan_probe_rate.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
     lib.selscan_probe_rate.restype = i32
     if path is None:
@@ -96,6 +99,11 @@ def selscan_last_cuda_error() -> int:
 def selscan_device_status(reset: bool = False) -> int:
     """0 if no kernel gave up a bounded wait since the last reset (synchronous read)."""
     return load_library().selscan_device_status(int(bool(reset)))
+
+
+def selscan_last_launch_count() -> int:
+    """Kernels enqueued by the last entry-point call on this host thread (see include/selscan.h)."""
+    return load_library().selscan_last_launch_count()
 
 
 def selscan_probe_rate(unit: str) -> float:
@@ -310,5 +318,5 @@ def selscan_step(u, delta, A, B, C, state, D=None, z=None, delta_bias=None, delt
 
 __all__ = ["selscan_fwd", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step",
            "selscan_status_string", "selscan_abi_version", "selscan_last_cuda_error", "selscan_device_status",
-           "selscan_probe_rate", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED",
+           "selscan_probe_rate", "selscan_last_launch_count", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED",
            "PROBE_UNITS"]

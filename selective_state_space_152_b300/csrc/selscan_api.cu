@@ -133,6 +133,8 @@ selscan_status_t check_args(const Span* ins, const bool* required_in, const size
 }  // namespace
 
 namespace selscan {
+thread_local int t_launches = 0;
+void count_launches(int n) { t_launches += n; }
 void* tensor_map_encoder() {
   std::call_once(g_range_once, init_range_query);
   return g_encode_tiled;
@@ -150,6 +152,7 @@ selscan_status_t prepare_fwd(const selscan_shape_t* shape, const void* u, const 
                              const float* conv_w, const float* conv_b, cudaStream_t s, selscan::FwdParams* p,
                              bool* done) {
   *done = false;
+  selscan::t_launches = 0;
   if (conv && !conv_w) return SELSCAN_ERR_NULL;
   selscan_status_t st = check_shape(shape);
   if (st != SELSCAN_OK) return st;
@@ -321,6 +324,7 @@ selscan_status_t selscan_step(const selscan_shape_t* shape, const void* u, const
                               const void* B, const void* C, const float* D, const void* z,
                               const float* delta_bias, int delta_softplus, float* state, void* out,
                               void* stream) {
+  selscan::t_launches = 0;
   selscan_status_t st = check_shape(shape);
   if (st != SELSCAN_OK) return st;
   if (shape->seqlen != 1) return SELSCAN_ERR_SHAPE;
@@ -389,5 +393,7 @@ int selscan_device_status(int reset) {
 }
 
 int selscan_abi_version(void) { return SELSCAN_ABI_VERSION; }
+
+int selscan_last_launch_count(void) { return selscan::t_launches; }
 
 }  // extern "C"

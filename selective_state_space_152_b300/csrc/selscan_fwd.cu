@@ -488,6 +488,7 @@ cudaError_t launch_kernel(const FwdParams& p, const TmaMaps& maps, cudaStream_t 
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>((p.dim + C::ROWS - 1) / C::ROWS), static_cast<unsigned>(p.batch));
   kern<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -668,36 +668,32 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
                   static_cast<unsigned>(p.nblocks));
   if (p.nblocks == 1) {
     scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+    count_launches(1);
     return cudaGetLastError();
   }
-  // Stream-ordered scratch for the block summaries and start states, released on the same stream.
-  // Time blocks only add parallelism: if the scratch cannot be had (no memory pool on the device, or
-  // the pool is exhausted), the same result (up to rounding) comes from one pass without it.
+  // Stream-ordered scratch for the block summaries and start states, released on the same stream.  If
+  // the pool cannot supply it the call fails with the allocation error (selscan_fwd_noalloc needs none).
   const int64_t N = p.dstate;
   const size_t summ_floats = static_cast<size_t>(p.nblocks - 1) * rows * (N + 1);
   const size_t start_floats = static_cast<size_t>(p.nblocks) * rows * N;
   void* ws = nullptr;
   e = cudaMallocAsync(&ws, (summ_floats + start_floats) * sizeof(float), s);
-  if (e != cudaSuccess) {
-    (void)cudaGetLastError();  // clear the allocation error
-    p.tblock = p.seqlen;
-    p.nblocks = 1;
-    const dim3 grid1(grid.x, grid.y, 1);
-    scan<<<grid1, R * 32, C::kSmem, s>>>(p, maps);
-    return cudaGetLastError();
-  }
+  if (e != cudaSuccess) return e;
   p.summ = static_cast<float*>(ws);
   p.start = p.summ + summ_floats;
   const dim3 sgrid(grid.x, grid.y, grid.z - 1);
   summary<<<sgrid, R * 32, C::kSmem, s>>>(p, maps);
+  count_launches(1);
   e = cudaGetLastError();
   if (e == cudaSuccess) {
     const int64_t threads = static_cast<int64_t>(rows) * N;
     selscan_carry_kernel<REV><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(p);
+    count_launches(1);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
     scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+    count_launches(1);
     e = cudaGetLastError();
   }
   const cudaError_t ef = cudaFreeAsync(ws, s);
@@ -809,6 +805,7 @@ cudaError_t launch_seq_noalloc_cfg(const FwdParams& p_in, cudaStream_t s, bool* 
                   static_cast<unsigned>(p.nblocks));
   if (p.nblocks == 1) {  // one pass: no scratch needed
     scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+    count_launches(1);
     return cudaGetLastError();
   }
   const int64_t N = p.dstate;
@@ -828,14 +825,17 @@ cudaError_t launch_seq_noalloc_cfg(const FwdParams& p_in, cudaStream_t s, bool* 
   p.start = ws + summ_floats;
   const dim3 sgrid(grid.x, grid.y, grid.z - 1);
   summary<<<sgrid, R * 32, C::kSmem, s>>>(p, maps);
+  count_launches(1);
   e = cudaGetLastError();
   if (e == cudaSuccess) {
     const int64_t threads = static_cast<int64_t>(rows) * N;
     selscan_carry_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(p);
+    count_launches(1);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
     scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
+    count_launches(1);
     e = cudaGetLastError();
   }
   return e;

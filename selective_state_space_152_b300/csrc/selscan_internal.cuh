@@ -105,6 +105,10 @@ cudaError_t launch_fwd_seq_ex(const FwdParams& p, selscan_dtype_t in_dtype, sels
 // allocation).  Sets *too_big and enqueues nothing if the problem needs more than the array holds.
 cudaError_t launch_fwd_seq_noalloc(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype,
                                    cudaStream_t s, bool* too_big);
+// Kernels enqueued by the current entry-point call on this host thread (read by
+// selscan_last_launch_count()); every launcher adds its launches.
+void count_launches(int n);
+
 // Read (and optionally clear) the device-side failure words set by a kernel's bounded wait.
 cudaError_t read_device_error(int* value, int reset);
 cudaError_t read_seq_device_error(int* value, int reset);

@@ -1034,6 +1034,7 @@ cudaError_t launch_rows_cfg(const FwdParams& p_in, const RowsPlan& plan, cudaStr
   const int threads = (p.warps + 1) * 32;
   if (p.nblocks == 1) {
     scan<<<grid, threads, smem, s>>>(p, maps);
+    count_launches(1);
     return cudaGetLastError();
   }
   const int64_t N = p.dstate;
@@ -1071,6 +1072,7 @@ cudaError_t launch_rows_cfg(const FwdParams& p_in, const RowsPlan& plan, cudaStr
     scan<<<grid, threads, smem, s>>>(p, maps);
     e = cudaGetLastError();
   }
+  count_launches(3);
   if (src == ScratchSource::Pool) {
     const cudaError_t ef = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = ef;

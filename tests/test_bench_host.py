@@ -20,6 +20,7 @@ def test_fwd_work_counts_the_bench_workload():
     h_last = 8 * 1536 * 16 * 4
     assert w["bytes"] == elems * per_elem + bc + small + h_last == 253_603_840
     assert w["mufu"] == elems * 20 and w["fp32"] == elems * 72
+    assert w["sfu"] == {"ex2": elems * 18, "lg2": elems, "rcp": elems}
 
 
 def test_step_work_counts_the_decode_workload():
@@ -32,7 +33,10 @@ def test_roofline_picks_the_slowest_resource():
     w = bench.fwd_work(8, 1536, 2048, 16)
     t = bench.roofline_times(w, sms=148, hbm_gbs=6516.4, sm_mhz=2032.0)
     assert t["mufu"] > t["fp32"] > t["hbm"]
-    assert abs(t["mufu"] * 1e6 - 52.30) < 0.05
+    # N + 2 exponentials at 32 per clock per SM, the logarithm and the reciprocal at 16
+    elems = 8 * 1536 * 2048
+    want = elems * (18 / 32 + 1 / 16 + 1 / 16) / (148 * 2.032e9)
+    assert abs(t["mufu"] - want) < 1e-12 and abs(t["mufu"] * 1e6 - 57.53) < 0.05
     e = bench.roofline_entry(w, t_kernel=2 * t["mufu"], sms=148, hbm_gbs=6516.4, sm_mhz=2032.0)
     assert e["bound"] == "alu" and e["resource"] == "mufu" and e["unit"] == "TFLOP/s"
     assert abs(e["frac"] - 0.5) < 1e-12

@@ -364,6 +364,29 @@ def test_decode_step_workload_full():
     check_h(hs, href, what="decode state after 64 steps")
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_step_rows_spanning_batch_entries(dt):
+    """The one-thread-per-row decode kernel with 300 channels: CTAs of 256 rows span two batch entries,
+    whose B and C each CTA stages separately; 5 steps carrying the state, against the forward oracle."""
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    inp = si.random_case(131, 3, 300, 5, 16, in_dtype=dt)
+    ref, href = oracle.selscan_fwd(inp)
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    state = t["h0"].clone()
+    outs = []
+    for s in range(5):
+        outs.append(ss.selscan_step(t["u"][..., s].contiguous(), t["delta"][..., s].contiguous(), t["A"],
+                                    t["B"][..., s].contiguous(), t["C"][..., s].contiguous(), state, D=t["D"],
+                                    z=t["z"][..., s].contiguous(), delta_bias=t["delta_bias"]))
+    torch.cuda.synchronize()
+    got = torch.stack(outs, dim=-1).cpu().numpy().astype(np.float64)
+    check_out(got, ref, dt, what="decode rows spanning batch entries")
+    check_h(state.cpu().numpy().astype(np.float64), href, what="decode state")
+
+
 def test_step_small_fp32_odd_dstate():
     import torch
 
