@@ -48,6 +48,9 @@ def _bind(lib):
     lib.oracle_conv_silu.argtypes = [i64, i64, i64, i64, i32, p, p, p, p]
     lib.oracle_conv_silu.restype = i32
     lib.oracle_selscan_fwd.restype = i32
+    lib.oracle_selscan_bwd.argtypes = [i64, i64, i64, i64, i32, p, p, p, p, p, p, p, p, i32, p, p, p, p, p, p, p, p,
+                                       p, p, p, p, i32]
+    lib.oracle_selscan_bwd.restype = i32
     lib.oracle_selscan_step.argtypes = [i64, i64, i64, i32, p, p, p, p, p, p, p, p, i32, p, p]
     lib.oracle_selscan_step.restype = i32
     lib.oracle_softplus.argtypes = [ctypes.c_double]
@@ -123,6 +126,38 @@ def selscan_fwd(inp: Dict[str, object], delta_softplus: bool = True, rows: Optio
     if rc != 0:
         raise ValueError("oracle_selscan_fwd rejected its arguments")
     return out, hl
+
+
+def selscan_bwd(inp: Dict[str, object], dout: np.ndarray, dh_last: Optional[np.ndarray] = None,
+                delta_softplus: bool = True, nthreads: Optional[int] = None, lib=None) -> Dict[str, np.ndarray]:
+    """Gradients of the fp64 forward for a loss with gradient ``dout`` [B, D, L] with respect to out and
+    ``dh_last`` [B, D, N] (or None: zero) with respect to h_last.
+
+    Returns float64 arrays keyed "u", "delta", "z" (None without z), "A", "B", "C", "D", "delta_bias"
+    (None when the input is absent) and "h0" (the gradient with respect to the start state, returned
+    also when h0 is absent, i.e. zero).
+    """
+    lib = lib or load()
+    Bsz, Dm, L, N = inp["shape"]
+    dt = inp["in_dtype"]
+    u, delta, z = _in(inp["u"], dt), _in(inp["delta"], dt), _in(inp.get("z"), dt)
+    Bm, Cm = _in(inp["B"], dt), _in(inp["C"], dt)
+    A, D, bias, h0 = _f32(inp["A"]), _f32(inp.get("D")), _f32(inp.get("delta_bias")), _f32(inp.get("h0"))
+    go = np.ascontiguousarray(dout, dtype=np.float64)
+    gh = None if dh_last is None else np.ascontiguousarray(dh_last, dtype=np.float64)
+    res = {"u": np.zeros((Bsz, Dm, L)), "delta": np.zeros((Bsz, Dm, L)),
+           "z": None if z is None else np.zeros((Bsz, Dm, L)), "A": np.zeros((Dm, N)),
+           "B": np.zeros((Bsz, N, L)), "C": np.zeros((Bsz, N, L)),
+           "D": None if D is None else np.zeros(Dm), "delta_bias": None if bias is None else np.zeros(Dm),
+           "h0": np.zeros((Bsz, Dm, N))}
+    nth = nthreads if nthreads is not None else (os.cpu_count() or 1)
+    rc = lib.oracle_selscan_bwd(Bsz, Dm, L, N, _DT[dt], _ptr(u), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D),
+                                _ptr(z), _ptr(bias), int(bool(delta_softplus)), _ptr(h0), _ptr(go), _ptr(gh),
+                                _ptr(res["u"]), _ptr(res["delta"]), _ptr(res["z"]), _ptr(res["A"]), _ptr(res["B"]),
+                                _ptr(res["C"]), _ptr(res["D"]), _ptr(res["delta_bias"]), _ptr(res["h0"]), int(nth))
+    if rc != 0:
+        raise ValueError("oracle_selscan_bwd rejected its arguments or ran out of memory")
+    return res
 
 
 def conv_silu(x, w, cb, in_dtype: str, lib=None) -> np.ndarray:

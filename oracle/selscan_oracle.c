@@ -1,5 +1,6 @@
 /*
- * fp64 CPU oracle for the selective-scan forward and the recurrent decode step.
+ * fp64 CPU oracle for the selective-scan forward, its gradients (backward) and the
+ * recurrent decode step.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
  * the CPU-baseline leg of the benchmark may load this library.  It shares no
@@ -233,6 +234,217 @@ int oracle_selscan_step(int64_t batch, int64_t dim, int64_t dstate, int in_dtype
     }
   }
   return 0;
+}
+
+/*
+ * Gradients of the forward (Δ·B discretisation, forward direction) for a loss whose gradient with
+ * respect to out is dout [B, D, L] and with respect to h_last is dh_last [B, D, N] (NULL: zero).
+ *
+ * Reverse-mode differentiation of the recurrence above, taken in the reverse of the order it runs.
+ * The forward of a row is first rerun keeping every state h_t (the pages' "recomputation": the
+ * backward needs the states, which the forward does not store).  Then, with g the gradient with
+ * respect to the state after the step being undone (starting from dh_last), for t = L-1 down to 0:
+ *   y_t = Σ_n C_t[n] h_t[n] + D u_t,  out_t = y_t · silu(z_t)
+ *     dy_t  = dout_t · silu(z_t)                      (dout_t without a gate)
+ *     dz_t  = dout_t · y_t · silu'(z_t),  silu'(z) = σ(z)(1 + z(1 - σ(z)))
+ *     dD   += dy_t · u_t,   du_t = dy_t · D
+ *   for every state n, with G = g[n] + dy_t C_t[n] the full gradient with respect to h_t[n]:
+ *     dC_t[n] += dy_t · h_t[n]
+ *     h_t[n] = Ā_t[n] h_{t-1}[n] + Δ_t B_t[n] u_t, Ā_t[n] = exp(Δ_t A[n]):
+ *       dB_t[n] += G Δ_t u_t,  du_t += G Δ_t B_t[n]
+ *       dΔ_t    += G (B_t[n] u_t + A[n] Ā_t[n] h_{t-1}[n])
+ *       dA[n]   += G Ā_t[n] h_{t-1}[n] Δ_t
+ *       g[n]     = G Ā_t[n]                         (the gradient with respect to h_{t-1}[n])
+ *   Δ_t = softplus(x_t), x_t = δ_t + Δ_bias:  dδ_t = dΔ_t σ(x_t) (dΔ_t without softplus), dΔ_bias += dδ_t
+ * and finally dh0 = g.  B and C are shared by the channels of a batch entry and A, D, Δ_bias by the
+ * batch entries of a channel, so their gradients are sums over those rows.
+ *
+ * Outputs are fp64: du, ddelta, dz [B, D, L] (dz may be NULL when z is), dA [D, N], dB, dC [B, N, L],
+ * dD, dbias [D] (each may be NULL), dh0 [B, D, N] (may be NULL).  Sums over rows are formed per worker
+ * thread (rows are dealt to workers in a fixed order) and added in worker order.
+ */
+typedef struct {
+  int64_t batch, dim, seqlen, dstate;
+  int in_dtype;
+  const void *u, *delta, *z, *B, *C;
+  const float *A, *D, *delta_bias, *h0;
+  int delta_softplus;
+  const double *dout, *dh_last;
+  double *du, *ddelta, *dz, *dh0;
+  int nthreads;
+} bwd_job;
+
+typedef struct {
+  const bwd_job* j;
+  int worker;
+  double *dA, *dB, *dC, *dD, *dbias; /* this worker's partial sums */
+  int failed;
+} bwd_worker_t;
+
+static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+static void bwd_row(bwd_worker_t* w, int64_t b, int64_t d, double* hs, double* ys) {
+  const bwd_job* j = w->j;
+  const int64_t L = j->seqlen, N = j->dstate, Dm = j->dim;
+  const double bias = j->delta_bias ? 1.0 * j->delta_bias[d] : 0.0;
+  const double Dd = j->D ? 1.0 * j->D[d] : 0.0;
+  /* Recomputation: hs[(t + 1) * N + n] = h_t[n] for t = -1 .. L-1, ys[t] = y_t. */
+  for (int64_t n = 0; n < N; n++) hs[n] = j->h0 ? (double)j->h0[(b * Dm + d) * N + n] : 0.0;
+  for (int64_t t = 0; t < L; t++) {
+    const int64_t e = (b * Dm + d) * L + t;
+    const double u = load_in(j->u, e, j->in_dtype);
+    const double x = bias + load_in(j->delta, e, j->in_dtype);
+    const double dt = j->delta_softplus ? softplus(x) : x;
+    double y = Dd * u;
+    for (int64_t n = 0; n < N; n++) {
+      const int64_t bc = (b * N + n) * L + t;
+      const double abar = exp(dt * (double)j->A[d * N + n]);
+      const double h = abar * hs[t * N + n] + dt * load_in(j->B, bc, j->in_dtype) * u;
+      hs[(t + 1) * N + n] = h;
+      y += load_in(j->C, bc, j->in_dtype) * h;
+    }
+    ys[t] = y;
+  }
+  /* The reverse sweep. */
+  double g[64];
+  for (int64_t n = 0; n < N; n++) g[n] = j->dh_last ? j->dh_last[(b * Dm + d) * N + n] : 0.0;
+  for (int64_t t = L - 1; t >= 0; t--) {
+    const int64_t e = (b * Dm + d) * L + t;
+    const double u = load_in(j->u, e, j->in_dtype);
+    const double x = bias + load_in(j->delta, e, j->in_dtype);
+    const double dt = j->delta_softplus ? softplus(x) : x;
+    double dy = j->dout[e];
+    if (j->z) {
+      const double zz = load_in(j->z, e, j->in_dtype);
+      const double sg = sigmoid(zz);
+      if (j->dz) j->dz[e] = j->dout[e] * ys[t] * sg * (1.0 + zz * (1.0 - sg));
+      dy = j->dout[e] * zz * sg;
+    }
+    if (w->dD) w->dD[d] += dy * u;
+    double du = dy * Dd, ddt = 0.0;
+    for (int64_t n = 0; n < N; n++) {
+      const int64_t bc = (b * N + n) * L + t;
+      const double Bv = load_in(j->B, bc, j->in_dtype), Cv = load_in(j->C, bc, j->in_dtype);
+      const double a = j->A[d * N + n];
+      const double abar = exp(a * dt); /* Ā_t[n] */
+      const double hprev = hs[t * N + n];
+      const double G = g[n] + dy * Cv;
+      if (w->dC) w->dC[bc] += dy * hs[(t + 1) * N + n];
+      if (w->dB) w->dB[bc] += G * dt * u;
+      du += G * dt * Bv;
+      ddt += G * (Bv * u + a * abar * hprev);
+      if (w->dA) w->dA[d * N + n] += G * abar * hprev * dt;
+      g[n] = G * abar;
+    }
+    const double dx = j->delta_softplus ? ddt * sigmoid(x) : ddt;
+    j->du[e] = du;
+    j->ddelta[e] = dx;
+    if (w->dbias) w->dbias[d] += dx;
+  }
+  if (j->dh0)
+    for (int64_t n = 0; n < N; n++) j->dh0[(b * Dm + d) * N + n] = g[n];
+}
+
+static void* bwd_worker(void* arg) {
+  bwd_worker_t* w = (bwd_worker_t*)arg;
+  const bwd_job* j = w->j;
+  const int64_t L = j->seqlen, N = j->dstate;
+  double* hs = (double*)malloc(sizeof(double) * (size_t)((L + 1) * N));
+  double* ys = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+  if (!hs || !ys) {
+    w->failed = 1;
+  } else {
+    for (int64_t r = w->worker; r < j->batch * j->dim; r += j->nthreads) bwd_row(w, r / j->dim, r % j->dim, hs, ys);
+  }
+  free(hs);
+  free(ys);
+  return NULL;
+}
+
+int oracle_selscan_bwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype, const void* u,
+                       const void* delta, const float* A, const void* B, const void* C, const float* D,
+                       const void* z, const float* delta_bias, int delta_softplus, const float* h0,
+                       const double* dout, const double* dh_last, double* du, double* ddelta, double* dz,
+                       double* dA, double* dB, double* dC, double* dD, double* dbias, double* dh0, int nthreads) {
+  if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1 || dstate > 64) return -1;
+  if (in_dtype != ORACLE_F32 && in_dtype != ORACLE_BF16) return -1;
+  if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta) return -1;
+  bwd_job j;
+  memset(&j, 0, sizeof j);
+  j.batch = batch;
+  j.dim = dim;
+  j.seqlen = seqlen;
+  j.dstate = dstate;
+  j.in_dtype = in_dtype;
+  j.u = u;
+  j.delta = delta;
+  j.z = z;
+  j.B = B;
+  j.C = C;
+  j.A = A;
+  j.D = D;
+  j.delta_bias = delta_bias;
+  j.h0 = h0;
+  j.delta_softplus = delta_softplus;
+  j.dout = dout;
+  j.dh_last = dh_last;
+  j.du = du;
+  j.ddelta = ddelta;
+  j.dz = dz;
+  j.dh0 = dh0;
+  j.nthreads = nthreads > 1 ? nthreads : 1;
+  const int nw = j.nthreads;
+  const size_t nbc = (size_t)(batch * dstate * seqlen), na = (size_t)(dim * dstate), nd = (size_t)dim;
+  bwd_worker_t* ws = (bwd_worker_t*)calloc((size_t)nw, sizeof(bwd_worker_t));
+  if (!ws) return -2;
+  int rc = 0;
+  for (int k = 0; k < nw; k++) {
+    ws[k].j = &j;
+    ws[k].worker = k;
+    ws[k].dA = dA ? (double*)calloc(na, sizeof(double)) : NULL;
+    ws[k].dB = dB ? (double*)calloc(nbc ? nbc : 1, sizeof(double)) : NULL;
+    ws[k].dC = dC ? (double*)calloc(nbc ? nbc : 1, sizeof(double)) : NULL;
+    ws[k].dD = dD ? (double*)calloc(nd ? nd : 1, sizeof(double)) : NULL;
+    ws[k].dbias = dbias ? (double*)calloc(nd ? nd : 1, sizeof(double)) : NULL;
+    if ((dA && !ws[k].dA) || (dB && !ws[k].dB) || (dC && !ws[k].dC) || (dD && !ws[k].dD) || (dbias && !ws[k].dbias))
+      rc = -2;
+  }
+  if (rc == 0) {
+    if (nw == 1) {
+      bwd_worker(&ws[0]);
+    } else {
+      pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nw);
+      int started = 0;
+      for (int k = 0; k < nw; k++)
+        if (pthread_create(&th[k], NULL, bwd_worker, &ws[k]) == 0) started++;
+        else break;
+      for (int k = started; k < nw; k++) bwd_worker(&ws[k]); /* any worker that could not start runs here */
+      for (int k = 0; k < started; k++) pthread_join(th[k], NULL);
+      free(th);
+    }
+    if (dA) memset(dA, 0, na * sizeof(double));
+    if (dB) memset(dB, 0, nbc * sizeof(double));
+    if (dC) memset(dC, 0, nbc * sizeof(double));
+    if (dD) memset(dD, 0, nd * sizeof(double));
+    if (dbias) memset(dbias, 0, nd * sizeof(double));
+    for (int k = 0; k < nw; k++) {
+      if (ws[k].failed) rc = -2;
+      for (size_t i = 0; dA && i < na; i++) dA[i] += ws[k].dA[i];
+      for (size_t i = 0; dB && i < nbc; i++) dB[i] += ws[k].dB[i];
+      for (size_t i = 0; dC && i < nbc; i++) dC[i] += ws[k].dC[i];
+      for (size_t i = 0; dD && i < nd; i++) dD[i] += ws[k].dD[i];
+      for (size_t i = 0; dbias && i < nd; i++) dbias[i] += ws[k].dbias[i];
+    }
+  }
+  for (int k = 0; k < nw; k++) {
+    free(ws[k].dA);
+    free(ws[k].dB);
+    free(ws[k].dC);
+    free(ws[k].dD);
+    free(ws[k].dbias);
+  }
+  free(ws);
+  return rc;
 }
 
 /* Scalar helpers exposed for pinning the oracle's own building blocks. */

@@ -41,6 +41,7 @@
 // layer); ZOH uses the exact zero-order-hold input factor (exp(ΔA) - 1)/A·B instead of Δ·B
 // ("Mamba架构与SSM模型：高效序列建模技术解析" §2.1); CONV computes u in the kernel from x by the block's
 // causal depthwise convolution of width 4 and SiLU (§3.2 of the same page, d_conv = 4).
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -1032,6 +1033,10 @@ cudaError_t launch_rows_cfg(const FwdParams& p_in, const RowsPlan& plan, cudaStr
   const dim3 grid(static_cast<unsigned>((p.dim + ROWS - 1) / ROWS), static_cast<unsigned>(p.batch),
                   static_cast<unsigned>(p.nblocks));
   const int threads = (p.warps + 1) * 32;
+  if (const char* dbg = getenv("SELSCAN_DEBUG_PLAN"); dbg && dbg[0] == '1')  // for tuning runs
+    fprintf(stderr, "selscan rows plan: states/lane %d, lanes/row %d, warps %d, stages %d, time blocks %d x %lld, "
+                    "grid %u x %u x %u, smem %zu, cost %.3g\n", SPL, G::Q, p.warps, p.stages, p.nblocks,
+            static_cast<long long>(p.tblock), grid.x, grid.y, grid.z, smem, plan.cost);
   if (p.nblocks == 1) {
     scan<<<grid, threads, smem, s>>>(p, maps);
     count_launches(1);

@@ -467,7 +467,112 @@ def pin_conv_feeds_scan(lib):
     assert np.array_equal(a, b) and np.array_equal(ah, bh), "u_f64 must replace u exactly"
 
 
+# ---- the backward (gradients) -------------------------------------------------------------------
+#
+# The pages describe training with the states recomputed in the backward pass instead of stored
+# ("Mamba状态空间模型深度解析：挑战Transformer的下一代序列建模范式" §2.2); the gradients themselves are
+# fixed by the forward.  Three independent routes pin them: central differences of the forward oracle,
+# the transpose of the materialised causal matrix (the forward is linear in u and h0 for fixed Δ), and
+# suffix sums in the prefix-sum special case.
+
+def _fd_loss(inp, w, v, lib, delta_softplus):
+    out, hl = oracle.selscan_fwd(inp, delta_softplus=delta_softplus, lib=lib, nthreads=1)
+    return float(np.sum(w * out) + np.sum(v * hl))
+
+
+def pin_bwd_finite_differences(lib):
+    """Every gradient == central differences of the forward oracle, L = Σ w·out + Σ v·h_last."""
+    rng = np.random.default_rng(41)
+    for seed, shape, sp in [(11, (2, 3, 10, 3), True), (12, (1, 2, 9, 2), False)]:
+        inp = _case(seed, *shape)
+        if not sp:  # keep Δ = δ positive without softplus
+            inp["delta_bias"] = None
+            inp["delta"] = (np.abs(inp["delta"]) * 0.05 + 0.01).astype(np.float32)
+        Bsz, Dm, L, N = shape
+        w = rng.standard_normal((Bsz, Dm, L))
+        v = rng.standard_normal((Bsz, Dm, N))
+        g = oracle.selscan_bwd(inp, w, dh_last=v, delta_softplus=sp, lib=lib, nthreads=1)
+        for name in ("u", "delta", "z", "A", "B", "C", "D", "delta_bias", "h0"):
+            arr = inp.get(name)
+            if arr is None:
+                continue
+            arr = np.asarray(arr, dtype=np.float32)
+            flat = np.arange(arr.size)
+            pick = flat if arr.size <= 24 else rng.choice(flat, size=12, replace=False)
+            for i in pick:
+                x = float(arr.flat[i])
+                hstep = 2.0 ** -12 * 2.0 ** max(0, math.floor(math.log2(abs(x) + 1.0)))
+                vals = []
+                for sgn in (1.0, -1.0):
+                    a2 = arr.copy()
+                    a2.flat[i] = np.float32(x + sgn * hstep)
+                    vals.append((float(a2.flat[i]), _fd_loss(dict(inp, **{name: a2}), w, v, lib, sp)))
+                fd = (vals[0][1] - vals[1][1]) / (vals[0][0] - vals[1][0])
+                got = float(g[name].flat[i])
+                scale = float(np.max(np.abs(g[name]))) + 1e-12
+                if not abs(got - fd) <= 2e-5 * scale + 1e-6 * abs(fd):
+                    raise AssertionError(f"d{name}[{i}] {shape}: oracle {got!r}, central difference {fd!r}")
+
+
+def pin_bwd_adjoint_matrix(lib):
+    """du and dh0 == the transposes of the materialised maps u -> (out, h_last) and h0 -> (out, h_last)."""
+    rng = np.random.default_rng(43)
+    for seed, shape in [(13, (2, 2, 14, 3)), (14, (1, 3, 9, 1))]:
+        inp = _case(seed, *shape, has_z=False)
+        Bsz, Dm, L, N = shape
+        w = rng.standard_normal((Bsz, Dm, L))
+        v = rng.standard_normal((Bsz, Dm, N))
+        g = oracle.selscan_bwd(inp, w, dh_last=v, lib=lib, nthreads=1)
+        x = np.asarray(inp["delta"], np.float64) + np.asarray(inp["delta_bias"], np.float64)[None, :, None]
+        dt = _softplus_lib(x)
+        Bm, Cm = np.asarray(inp["B"], np.float64), np.asarray(inp["C"], np.float64)
+        A, Dv = np.asarray(inp["A"], np.float64), np.asarray(inp["D"], np.float64)
+        tri = np.tril(np.ones((L, L), dtype=bool))
+        for b in range(Bsz):
+            for d in range(Dm):
+                S = np.cumsum(dt[b, d])
+                M = np.diag(np.full(L, Dv[d]))
+                du_hl = np.zeros(L)
+                dh0 = np.zeros(N)
+                for n in range(N):
+                    decay = np.where(tri, np.exp(A[d, n] * np.where(tri, S[:, None] - S[None, :], 0.0)), 0.0)
+                    M = M + Cm[b, n][:, None] * decay * (dt[b, d] * Bm[b, n])[None, :]
+                    Hrow = np.exp(A[d, n] * (S[-1] - S)) * dt[b, d] * Bm[b, n]  # u_s -> h_last[n]
+                    du_hl += Hrow * v[b, d, n]
+                    dh0[n] = np.sum(Cm[b, n] * np.exp(A[d, n] * S) * w[b, d]) + np.exp(A[d, n] * S[-1]) * v[b, d, n]
+                _rel_close(g["u"][b, d], M.T @ w[b, d] + du_hl, 1e-10, what=f"du adjoint {shape}")
+                _rel_close(g["h0"][b, d], dh0, 1e-10, what=f"dh0 adjoint {shape}")
+
+
+def pin_bwd_prefix_sum(lib):
+    """A = 0, N = 1, no softplus, no gate: every gradient by suffix sums of the cumulative-sum model."""
+    inp = _case(15, 2, 3, 16, 1, has_z=False)
+    inp["A"] = np.zeros_like(inp["A"])
+    inp["delta_bias"] = None
+    rng = np.random.default_rng(44)
+    Bsz, Dm, L, _ = inp["shape"]
+    w = rng.standard_normal((Bsz, Dm, L))
+    v = rng.standard_normal((Bsz, Dm, 1))
+    # three worker threads over the six rows: the sums over rows are formed per worker and then added
+    g = oracle.selscan_bwd(inp, w, dh_last=v, delta_softplus=False, lib=lib, nthreads=3)
+    u = np.asarray(inp["u"], np.float64)
+    dt = np.asarray(inp["delta"], np.float64)
+    Bm, Cm = np.asarray(inp["B"], np.float64)[:, 0], np.asarray(inp["C"], np.float64)[:, 0]
+    Dv, h0 = np.asarray(inp["D"], np.float64), np.asarray(inp["h0"], np.float64)[..., 0]
+    h = h0[..., None] + np.cumsum(dt * Bm[:, None, :] * u, axis=-1)            # h_t
+    hprev = np.concatenate([h0[..., None], h[..., :-1]], axis=-1)              # h_{t-1}
+    R = np.flip(np.cumsum(np.flip(Cm[:, None, :] * w, -1), -1), -1) + v        # Σ_{t' ≥ t} C w + v
+    _rel_close(g["u"], dt * Bm[:, None, :] * R + Dv[None, :, None] * w, 1e-11, what="du prefix sum")
+    _rel_close(g["delta"], Bm[:, None, :] * u * R, 1e-11, what="ddelta prefix sum")
+    _rel_close(g["B"][:, 0], np.sum(dt * u * R, axis=1), 1e-11, what="dB prefix sum")
+    _rel_close(g["C"][:, 0], np.sum(w * h, axis=1), 1e-11, what="dC prefix sum")
+    _rel_close(g["D"], np.sum(w * u, axis=(0, 2)), 1e-11, what="dD prefix sum")
+    _rel_close(g["A"][:, 0], np.sum(R * hprev * dt, axis=(0, 2)), 1e-11, what="dA prefix sum")
+    _rel_close(g["h0"][..., 0], R[..., 0], 1e-11, what="dh0 prefix sum")
+
+
 ALL_PINS = [pin_brute_force, pin_lti_convolution, pin_delta_to_zero, pin_prefix_sum, pin_memoryless, pin_gate,
             pin_scalar_functions, pin_carry, pin_step_equals_fwd, pin_linearity, pin_causality,
             pin_worked_examples, pin_row_subset, pin_reverse_brute_force, pin_zoh_matches_ode, pin_zoh_limits,
-            pin_conv_silu, pin_conv_feeds_scan]
+            pin_conv_silu, pin_conv_feeds_scan, pin_bwd_finite_differences, pin_bwd_adjoint_matrix,
+            pin_bwd_prefix_sum]

@@ -61,6 +61,29 @@ MUTANTS = [
     ("step_no_gate", "if (z) y *= silu(load_in(z, e, in_dtype));", "if (0) y *= silu(load_in(z, e, in_dtype));"),
     ("step_bias_ignored", "x = load_in(delta, e, in_dtype) + (delta_bias ? (double)delta_bias[d] : 0.0);",
      "x = load_in(delta, e, in_dtype);"),
+    # the backward
+    ("bwd_sign_of_A_in_sweep", "exp(a * dt); /* Ā_t[n] */", "exp(-a * dt); /* Ā_t[n] */"),
+    ("bwd_recompute_sign_of_A", "const double abar = exp(dt * (double)j->A[d * N + n]);",
+     "const double abar = exp(-dt * (double)j->A[d * N + n]);"),
+    ("bwd_no_decay_of_g", "      g[n] = G * abar;\n", "      g[n] = G;\n"),
+    ("bwd_dC_with_h_prev", "w->dC[bc] += dy * hs[(t + 1) * N + n];", "w->dC[bc] += dy * hs[t * N + n];"),
+    ("bwd_dA_with_h_t", "w->dA[d * N + n] += G * abar * hprev * dt;", "w->dA[d * N + n] += G * abar * hs[(t + 1) * N + n] * dt;"),
+    ("bwd_dA_sign", "w->dA[d * N + n] += G * abar * hprev * dt;", "w->dA[d * N + n] -= G * abar * hprev * dt;"),
+    ("bwd_ddt_drops_decay_term", "ddt += G * (Bv * u + a * abar * hprev);", "ddt += G * Bv * u;"),
+    ("bwd_ddt_drops_input_term", "ddt += G * (Bv * u + a * abar * hprev);", "ddt += G * a * abar * hprev;"),
+    ("bwd_du_drops_D", "double du = dy * Dd, ddt = 0.0;", "double du = 0.0, ddt = 0.0;"),
+    ("bwd_du_drops_delta", "du += G * dt * Bv;", "du += G * Bv;"),
+    ("bwd_dB_uses_dy", "w->dB[bc] += G * dt * u;", "w->dB[bc] += dy * dt * u;"),
+    ("bwd_G_without_readout", "const double G = g[n] + dy * Cv;", "const double G = g[n];"),
+    ("bwd_softplus_derivative_missing", "ddt * sigmoid(x) : ddt;", "ddt : ddt;"),
+    ("bwd_dz_missing_silu_slope", "sg * (1.0 + zz * (1.0 - sg));", "sg;"),
+    ("bwd_dy_ungated", "dy = j->dout[e] * zz * sg;", "dy = j->dout[e];"),
+    ("bwd_dD_uses_dout", "if (w->dD) w->dD[d] += dy * u;", "if (w->dD) w->dD[d] += j->dout[e] * u;"),
+    ("bwd_dh_last_ignored", "g[n] = j->dh_last ? j->dh_last[(b * Dm + d) * N + n] : 0.0;", "g[n] = 0.0;"),
+    ("bwd_recompute_without_h0", "hs[n] = j->h0 ? (double)j->h0[(b * Dm + d) * N + n] : 0.0;", "hs[n] = 0.0;"),
+    ("bwd_dbias_uses_ddt", "if (w->dbias) w->dbias[d] += dx;", "if (w->dbias) w->dbias[d] += ddt;"),
+    ("bwd_reduction_drops_worker", "for (size_t i = 0; dB && i < nbc; i++) dB[i] += ws[k].dB[i];",
+     "for (size_t i = 0; dB && i < nbc && k == 0; i++) dB[i] += ws[k].dB[i];"),
 ]
 
 
