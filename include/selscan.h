@@ -62,6 +62,7 @@
 #ifndef SELSCAN_H_
 #define SELSCAN_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -82,7 +83,8 @@ typedef enum {
   SELSCAN_ERR_CUDA = 5,        /* a CUDA call failed; see selscan_last_cuda_error() */
   SELSCAN_ERR_POINTER = 6,     /* a pointer is not device-accessible or its extent leaves its allocation */
   SELSCAN_ERR_ALIAS = 7,       /* an output overlaps an input (other than h_last == h0) */
-  SELSCAN_ERR_SCRATCH = 8      /* selscan_fwd_noalloc only: the problem needs more scratch than its fixed buffer */
+  SELSCAN_ERR_SCRATCH = 8      /* the problem needs more scratch than the buffer it may use: selscan_fwd_noalloc's
+                                  fixed array, or the workspace given to selscan_bwd */
 } selscan_status_t;
 
 /* Problem sizes.  For selscan_step, seqlen must be 1. */
@@ -144,8 +146,8 @@ selscan_status_t selscan_step(const selscan_shape_t* shape, const void* u, const
  *                         B̄ = (ΔA)^{-1}(exp(ΔA) - I)·ΔB).
  *
  * Arguments, layouts, checks and errors are those of selscan_fwd.  flags = 0 computes exactly what
- * selscan_fwd computes.  Unknown flag bits return SELSCAN_ERR_UNSUPPORTED.  It always runs the
- * sequential kernel (with time blocks and their stream-ordered scratch for problems with few rows).
+ * selscan_fwd computes.  Unknown flag bits return SELSCAN_ERR_UNSUPPORTED.  It runs the kernels
+ * selscan_fwd runs (time blocks and their stream-ordered scratch for problems with few rows).
  */
 #define SELSCAN_FLAG_REVERSE 1u
 #define SELSCAN_FLAG_ZOH 2u
@@ -170,8 +172,8 @@ selscan_status_t selscan_fwd_ex(const selscan_shape_t* shape, const void* u, con
  *   flags   : 0 or SELSCAN_FLAG_ZOH (the front is causal: SELSCAN_FLAG_REVERSE is rejected with
  *             SELSCAN_ERR_UNSUPPORTED)
  * Every other argument, check and error is that of selscan_fwd.  A sequence split over calls
- * restarts the convolution from zero history at each call's first step.  It runs the sequential
- * kernel (with time blocks and their stream-ordered scratch for problems with few rows).
+ * restarts the convolution from zero history at each call's first step.  It runs the kernels
+ * selscan_fwd runs (time blocks and their stream-ordered scratch for problems with few rows).
  */
 selscan_status_t selscan_fwd_conv(const selscan_shape_t* shape, const void* x, const float* conv_w,
                                   const float* conv_b, const void* delta, const float* A, const void* B,
@@ -187,8 +189,8 @@ selscan_status_t selscan_fwd_conv(const selscan_shape_t* shape, const void* x, c
  * scratch from the CUDA memory pool for problems with few rows, see below.)  The pages describe no
  * such entry point; it is an engineering addition.
  *
- * It always runs the sequential kernel.  For problems with few rows that kernel cuts the sequence
- * into time blocks and keeps, per block, a summary and a start state of every row:
+ * It runs the kernels selscan_fwd runs.  For problems with few rows they cut the sequence into time
+ * blocks and keep, per block, a summary and a start state of every row:
  *   ((blocks - 1) * (N + 1) + blocks * N) * batch * dim floats.
  * These live in one fixed device array of SELSCAN_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library,
  * reserved on every GPU that loads the library until the process exits.  A problem that would need
@@ -205,6 +207,56 @@ selscan_status_t selscan_fwd_noalloc(const selscan_shape_t* shape, const void* u
                                      const void* B, const void* C, const float* D, const void* z,
                                      const float* delta_bias, int delta_softplus, const float* h0, void* out,
                                      float* h_last, void* stream);
+
+/*
+ * Gradients of selscan_fwd (the backward pass, for training): given dout = ∂loss/∂out and
+ * dh_last = ∂loss/∂h_last, the gradients of the loss with respect to every input.  Reverse-mode
+ * differentiation of the forward's recurrence, with g the gradient with respect to the state after the
+ * step being undone (g = dh_last after the last step), for t from L-1 down to 0:
+ *
+ *   dy_t = dout_t · silu(z_t),      dz_t = dout_t · y_t · σ(z_t)·(1 + z_t·(1 - σ(z_t)))
+ *   G[n] = g[n] + dy_t · C[b,n,t]
+ *   dC[b,n,t] = Σ_d dy_t · h_t[n]          dB[b,n,t] = Σ_d G[n] · Δ_t · u_t
+ *   du_t = dy_t · D[d] + Δ_t · Σ_n G[n]·B[b,n,t]
+ *   dΔ_t = Σ_n G[n] · (B[b,n,t]·u_t + A[d,n]·Ā_t[n]·h_{t-1}[n]),   dδ_t = dΔ_t · σ(δ_t + Δ_bias[d])
+ *   dA[d,n] += Σ_b Δ_t · G[n] · Ā_t[n] · h_{t-1}[n],    g[n] = G[n] · Ā_t[n]
+ *   dD[d] = Σ_{b,t} dy_t · u_t,   dΔ_bias[d] = Σ_{b,t} dδ_t,   dh0 = g after t = 0
+ *
+ * (σ is the logistic function, the derivative of softplus; with delta_softplus == 0, dδ_t = dΔ_t.)
+ * The forward's states are not stored: the kernel recomputes them, keeping only the state at the start
+ * of every 16-step chunk in `workspace` — the recomputation that "Mamba状态空间模型深度解析：挑战
+ * Transformer的下一代序列建模范式" §2.2 describes for training.
+ *
+ *   u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0 : the forward call's inputs (as selscan_fwd)
+ *   dout        : [B, D, L]  out_dtype   ∂loss/∂out
+ *   dh_last     : [B, D, N]  fp32        ∂loss/∂h_last (nullable: 0)
+ *   du, ddelta  : [B, D, L]  in_dtype    ∂loss/∂u, ∂loss/∂delta (written)
+ *   dz          : [B, D, L]  in_dtype    ∂loss/∂z (written; required when z is given, ignored otherwise)
+ *   dA          : [D, N]     fp32        ∂loss/∂A (overwritten)
+ *   dB, dC      : [B, N, L]  fp32        ∂loss/∂B, ∂loss/∂C (overwritten; fp32 whatever in_dtype is,
+ *                                        since they are sums over the D channels)
+ *   dD, ddelta_bias : [D]    fp32        (nullable: not computed; computed even when D or delta_bias is
+ *                                        NULL, as the gradient at 0)
+ *   dh0         : [B, D, N]  fp32        ∂loss/∂h0 (nullable; written also when h0 is NULL)
+ *   workspace   : device memory of at least selscan_bwd_workspace_size(shape) bytes, 16-byte aligned,
+ *                 used only while the call's work runs; NULL takes it from the CUDA memory pool of
+ *                 `stream` (cudaMallocAsync / cudaFreeAsync) instead.  A smaller workspace_bytes returns
+ *                 SELSCAN_ERR_SCRATCH.
+ *
+ * Accumulated gradients (dA, dB, dC, dD, ddelta_bias) are summed with floating-point atomics, so their
+ * last bits may differ from run to run.  No output may overlap an input, another output or the
+ * workspace.  The checks and errors are otherwise those of selscan_fwd; L = 0 or no rows writes zeros
+ * to the accumulated gradients and dh0 = dh_last (or 0).
+ */
+selscan_status_t selscan_bwd(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* delta_bias, int delta_softplus, const float* h0, const void* dout,
+                             const float* dh_last, void* du, void* ddelta, void* dz, float* dA, float* dB,
+                             float* dC, float* dD, float* ddelta_bias, float* dh0, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace selscan_bwd needs for `shape` (0 for an invalid shape). */
+size_t selscan_bwd_workspace_size(const selscan_shape_t* shape);
 
 /* Human-readable name of a status code (static storage). */
 const char* selscan_status_string(selscan_status_t status);
@@ -226,8 +278,8 @@ int selscan_abi_version(void);
 
 /*
  * The number of kernels that the last selscan_fwd, selscan_fwd_ex, selscan_fwd_conv,
- * selscan_fwd_noalloc or selscan_step call on this host thread enqueued: 1 for a
- * forward run in one pass or a decode step, 3 for a forward run in time blocks (the
+ * selscan_fwd_noalloc, selscan_bwd or selscan_step call on this host thread enqueued: 1 for a
+ * forward run in one pass, a backward or a decode step, 3 for a forward run in time blocks (the
  * summary pass, the carry pass and the scan), 0 when the call enqueued no kernel (an
  * argument error, no rows, or an empty sequence, whose state is passed on by a copy).
  * The pages have no counterpart; it lets a caller (or a benchmark) account for the

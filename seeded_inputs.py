@@ -205,3 +205,14 @@ def random_case(seed: int, batch: int, dim: int, seqlen: int, dstate: int, in_dt
         dt = np.exp(np.log(1e-3) + uu * (np.log(1e-1) - np.log(1e-3)))
         out["delta_bias"] = (dt + np.log(-np.expm1(-dt))).astype(np.float32)
     return out
+
+
+def random_cotangents(seed: int, batch: int, dim: int, seqlen: int, dstate: int, dout_dtype: str = "f32",
+                      has_dh_last: bool = True) -> Dict[str, object]:
+    """Seeded gradients of a loss with respect to the forward's outputs, for backward tests:
+    "dout" [B, D, L] (N(0,1), fp32 or bf16 bit patterns) and "dh_last" [B, D, N] (N(0,1) fp32 or None)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0xB4C])))
+    go = rng.standard_normal(size=(batch, dim, seqlen), dtype=np.float32)
+    return {"dout": f32_to_bf16_bits(go) if dout_dtype == "bf16" else go,
+            "dh_last": rng.standard_normal(size=(batch, dim, dstate), dtype=np.float32) if has_dh_last else None,
+            "dout_dtype": dout_dtype}

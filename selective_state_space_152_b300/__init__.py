@@ -1,4 +1,4 @@
-"""Python binding of libselscan (selective-scan forward and recurrent decode step on B300).
+"""Python binding of libselscan (selective-scan forward, its gradients and the recurrent decode step on B300).
 
 The functions here only marshal arguments: they check tensor types and
 layouts, allocate missing outputs with torch, and call the C ABI declared in
@@ -23,7 +23,7 @@ STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SE
           8: "SELSCAN_ERR_SCRATCH"}
 EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
             "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_probe_rate",
-            "selscan_last_launch_count")
+            "selscan_last_launch_count", "selscan_bwd", "selscan_bwd_workspace_size")
 # Units of selscan_probe_rate (include/selscan_probe.h).
 PROBE_UNITS = {"ex2": 0, "lg2": 1, "rcp": 2, "tanh": 3, "ffma": 4, "ffma2": 5}
 SELSCAN_FLAG_REVERSE, SELSCAN_FLAG_ZOH = 1, 2
@@ -77,6 +77,11 @@ def load_library(path: Optional[str] = None):
     lib.selscan_abi_version.restype = i32
     lib.selscan_last_launch_count.argtypes = []
     lib.selscan_last_launch_count.restype = i32
+    lib.selscan_bwd.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                vp, ctypes.c_size_t, vp]
+    lib.selscan_bwd.restype = i32
+    lib.selscan_bwd_workspace_size.argtypes = [shp]
+    lib.selscan_bwd_workspace_size.restype = ctypes.c_size_t
     lib.selscan_probe_rate.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
     lib.selscan_probe_rate.restype = i32
     if path is None:
@@ -316,7 +321,69 @@ def selscan_step(u, delta, A, B, C, state, D=None, z=None, delta_bias=None, delt
     return out
 
 
-__all__ = ["selscan_fwd", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step",
+def selscan_bwd_workspace_size(Bsz: int, Dm: int, L: int, N: int) -> int:
+    """Bytes of workspace ``selscan_bwd`` needs for a [Bsz, Dm, L] problem with N states."""
+    shape = SelscanShape(Bsz, Dm, L, N, SELSCAN_F32, SELSCAN_F32)
+    return int(load_library().selscan_bwd_workspace_size(ctypes.byref(shape)))
+
+
+def selscan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
+                dh_last=None, grads=None, workspace=None, stream=None, want_dh0: bool = True):
+    """Gradients of ``selscan_fwd`` for ``dout`` = ∂loss/∂out (and ``dh_last`` = ∂loss/∂h_last, or None).
+
+    Returns a dict with "u", "delta" and "z" ([B, D, L], u's dtype; "z" None without z), "A" [D, N],
+    "B", "C" ([B, N, L], float32), "D", "delta_bias" ([D], float32) and "h0" ([B, D, N], float32; None
+    unless ``want_dh0``).  ``grads`` may hold preallocated outputs under the same keys.  ``workspace`` is
+    a CUDA tensor of at least ``selscan_bwd_workspace_size`` bytes (or None: the library takes it from
+    the stream's memory pool).
+    """
+    torch = _torch()
+    lib = load_library()
+    if u.dim() != 3 or B.dim() != 3:
+        raise ValueError("u must be [B, D, L] and B must be [B, N, L]")
+    Bsz, Dm, L = u.shape
+    N = B.shape[1]
+    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias), ("h0", h0), ("dh_last", dh_last)):
+        _need_f32(name, t)
+    for name, t in (("delta", delta), ("z", z), ("B", B), ("C", C)):
+        if t is not None and t.dtype != u.dtype:
+            raise TypeError(f"{name} must have u's dtype {u.dtype}")
+    g = dict(grads or {})
+    dev = u.device
+
+    def out(key, shp, dt):
+        if g.get(key) is None:
+            g[key] = torch.empty(shp, device=dev, dtype=dt)
+
+    out("u", (Bsz, Dm, L), u.dtype)
+    out("delta", (Bsz, Dm, L), u.dtype)
+    if z is not None:
+        out("z", (Bsz, Dm, L), u.dtype)
+    else:
+        g["z"] = None
+    out("A", (Dm, N), torch.float32)
+    out("B", (Bsz, N, L), torch.float32)
+    out("C", (Bsz, N, L), torch.float32)
+    out("D", (Dm,), torch.float32)
+    out("delta_bias", (Dm,), torch.float32)
+    if want_dh0:
+        out("h0", (Bsz, Dm, N), torch.float32)
+    else:
+        g["h0"] = None
+    for key in ("A", "B", "C", "D", "delta_bias", "h0"):
+        _need_f32("grad of " + key, g.get(key))
+    shape = SelscanShape(Bsz, Dm, L, N, _dtype_code(u.dtype), _dtype_code(dout.dtype))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.selscan_bwd(ctypes.byref(shape), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                         _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(dh_last),
+                         _ptr(g["u"]), _ptr(g["delta"]), _ptr(g["z"]), _ptr(g["A"]), _ptr(g["B"]), _ptr(g["C"]),
+                         _ptr(g["D"]), _ptr(g["delta_bias"]), _ptr(g["h0"]), _ptr(workspace), ws_bytes,
+                         _stream_handle(stream))
+    _check(st)
+    return g
+
+
+__all__ = ["selscan_fwd", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step",
            "selscan_status_string", "selscan_abi_version", "selscan_last_cuda_error", "selscan_device_status",
            "selscan_probe_rate", "selscan_last_launch_count", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED",
            "PROBE_UNITS"]

@@ -320,6 +320,105 @@ selscan_status_t selscan_fwd_noalloc(const selscan_shape_t* shape, const void* u
   return too_big ? SELSCAN_ERR_SCRATCH : SELSCAN_OK;
 }
 
+size_t selscan_bwd_workspace_size(const selscan_shape_t* shape) {
+  if (check_shape(shape) != SELSCAN_OK) return 0;
+  int64_t rows, elems;
+  if (!mul_ok(shape->batch, shape->dim, &rows) || !mul_ok(rows, shape->seqlen, &elems) || elems > INT64_MAX / 16)
+    return 0;
+  return selscan::bwd_workspace_bytes(rows, shape->seqlen);
+}
+
+// The backward: the checks of the forward's inputs plus dout, dh_last and the gradient outputs, zeroing
+// of the accumulated gradients, then one kernel.
+selscan_status_t selscan_bwd(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* delta_bias, int delta_softplus, const float* h0, const void* dout,
+                             const float* dh_last, void* du, void* ddelta, void* dz, float* dA, float* dB,
+                             float* dC, float* dD, float* ddelta_bias, float* dh0, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  selscan::t_launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  selscan_status_t st = check_shape(shape);
+  if (st != SELSCAN_OK) return st;
+  if (z && !dz) return SELSCAN_ERR_NULL;
+  if (!z) dz = nullptr;
+  const int64_t Bsz = shape->batch, Dm = shape->dim, L = shape->seqlen, N = shape->dstate;
+  int64_t rows, elems, bcn, bc_elems, an, states;
+  if (!mul_ok(Bsz, Dm, &rows) || !mul_ok(rows, L, &elems) || !mul_ok(Bsz, N, &bcn) || !mul_ok(bcn, L, &bc_elems) ||
+      !mul_ok(Dm, N, &an) || !mul_ok(rows, N, &states))
+    return SELSCAN_ERR_SHAPE;
+  if (elems > INT64_MAX / 16 || bc_elems > INT64_MAX / 4 || states > INT64_MAX / 4) return SELSCAN_ERR_SHAPE;
+  if (Bsz > 65535) return SELSCAN_ERR_UNSUPPORTED;  // one grid row per batch entry
+  const size_t ei = dsize(shape->in_dtype), eo = dsize(shape->out_dtype);
+  const size_t ws_need = selscan::bwd_workspace_bytes(rows, L);
+  if (workspace && workspace_bytes < ws_need) return SELSCAN_ERR_SCRATCH;
+  const Span ins[] = {{u, elems * (int64_t)ei},    {delta, elems * (int64_t)ei}, {A, an * 4},
+                      {B, bc_elems * (int64_t)ei}, {C, bc_elems * (int64_t)ei},  {D, Dm * 4},
+                      {z, elems * (int64_t)ei},    {delta_bias, Dm * 4},         {h0, states * 4},
+                      {dout, elems * (int64_t)eo}, {dh_last, states * 4}};
+  const bool req_in[] = {true, true, true, true, true, false, false, false, false, true, false};
+  const size_t el_in[] = {ei, ei, 4, ei, ei, 4, ei, 4, 4, eo, 4};
+  const Span outs[] = {{du, elems * (int64_t)ei}, {ddelta, elems * (int64_t)ei}, {dz, elems * (int64_t)ei},
+                       {dA, an * 4},              {dB, bc_elems * 4},             {dC, bc_elems * 4},
+                       {dD, Dm * 4},              {ddelta_bias, Dm * 4},          {dh0, states * 4},
+                       {workspace, (int64_t)ws_need}};
+  const bool req_out[] = {true, true, false, true, true, true, false, false, false, false};
+  const size_t el_out[] = {ei, ei, ei, 4, 4, 4, 4, 4, 4, 16};
+  st = check_args(ins, req_in, el_in, 11, outs, req_out, el_out, 10, nullptr, nullptr);
+  if (st != SELSCAN_OK) return st;
+  // The accumulated gradients start from zero (stream-ordered fills, no allocation).
+  cudaError_t e = cudaSuccess;
+  const struct {
+    void* p;
+    int64_t bytes;
+  } zero[] = {{dA, an * 4}, {dB, bc_elems * 4}, {dC, bc_elems * 4}, {dD, Dm * 4}, {ddelta_bias, Dm * 4}};
+  for (const auto& zf : zero)
+    if (zf.p && zf.bytes > 0 && e == cudaSuccess) e = cudaMemsetAsync(zf.p, 0, zf.bytes, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (rows == 0) return SELSCAN_OK;
+  if (L == 0) {  // no steps: the state's gradient passes through unchanged
+    if (dh0) {
+      e = dh_last ? cudaMemcpyAsync(dh0, dh_last, states * 4, cudaMemcpyDeviceToDevice, s)
+                  : cudaMemsetAsync(dh0, 0, states * 4, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return SELSCAN_OK;
+  }
+  selscan::BwdParams p;
+  memset(&p, 0, sizeof p);
+  p.batch = Bsz;
+  p.dim = Dm;
+  p.seqlen = L;
+  p.dstate = static_cast<int>(N);
+  p.u = u;
+  p.delta = delta;
+  p.z = z;
+  p.B = B;
+  p.C = C;
+  p.A = A;
+  p.D = D;
+  p.delta_bias = delta_bias;
+  p.h0 = h0;
+  p.dout = dout;
+  p.dh_last = dh_last;
+  p.du = du;
+  p.ddelta = ddelta;
+  p.dz = dz;
+  p.dA = dA;
+  p.dB = dB;
+  p.dC = dC;
+  p.dD = dD;
+  p.ddelta_bias = ddelta_bias;
+  p.dh0 = dh0;
+  p.delta_softplus = delta_softplus != 0;
+  p.vec_in = aligned(u, 16) && aligned(delta, 16) && (!z || aligned(z, 16)) && L % (16 / ei) == 0;
+  p.vec_dout = aligned(dout, 16) && L % (16 / eo) == 0;
+  p.vec_grad = aligned(du, 4 * ei) && aligned(ddelta, 4 * ei) && (!dz || aligned(dz, 4 * ei)) && L % 4 == 0;
+  p.vec_dbc = aligned(dB, 16) && aligned(dC, 16) && L % 4 == 0;
+  e = selscan::launch_bwd(p, shape->in_dtype, shape->out_dtype, workspace, s);
+  return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
+}
+
 selscan_status_t selscan_step(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
                               const void* B, const void* C, const float* D, const void* z,
                               const float* delta_bias, int delta_softplus, float* state, void* out,
@@ -376,7 +475,8 @@ const char* selscan_status_string(selscan_status_t status) {
     case SELSCAN_ERR_POINTER: return "SELSCAN_ERR_POINTER: pointer not device-accessible or extent outside its allocation";
     case SELSCAN_ERR_ALIAS: return "SELSCAN_ERR_ALIAS: an output overlaps an input";
     case SELSCAN_ERR_SCRATCH:
-      return "SELSCAN_ERR_SCRATCH: the problem needs more time-block scratch than selscan_fwd_noalloc's fixed buffer";
+      return "SELSCAN_ERR_SCRATCH: the problem needs more scratch than the buffer it may use (selscan_fwd_noalloc's "
+             "fixed array, or selscan_bwd's workspace)";
   }
   return "unknown selscan status";
 }

@@ -70,6 +70,44 @@ struct StepParams {
 
 cudaError_t launch_fwd(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);
 
+// Arguments of one selscan_bwd launch, already validated on the host.
+struct BwdParams {
+  int64_t batch, dim, seqlen;
+  int dstate;
+  const void* u;
+  const void* delta;
+  const void* z;  // nullable
+  const void* B;
+  const void* C;
+  const float* A;
+  const float* D;           // nullable
+  const float* delta_bias;  // nullable
+  const float* h0;          // nullable
+  const void* dout;
+  const float* dh_last;  // nullable
+  void* du;
+  void* ddelta;
+  void* dz;  // required iff z is given
+  float* dA;
+  float* dB;
+  float* dC;
+  float* dD;           // nullable
+  float* ddelta_bias;  // nullable
+  float* dh0;          // nullable
+  float* ckpt;         // workspace: the state at the start of every chunk, [rows][chunks][16]
+  int delta_softplus;
+  int vec_in;    // u, delta, z rows may be read with 16-byte vectors
+  int vec_dout;  // dout rows may be read with 16-byte vectors
+  int vec_grad;  // du, ddelta, dz may be written four steps at a time (8- or 16-byte stores)
+  int vec_dbc;   // dB, dC may take 16-byte atomic adds
+};
+// Bytes of the backward's workspace (chunk checkpoints) for `rows` = batch * dim rows.
+size_t bwd_workspace_bytes(int64_t rows, int64_t seqlen);
+// The backward: zeroing of the accumulated gradients is the caller's; `workspace` (nullable: taken from
+// the stream's memory pool) holds at least bwd_workspace_bytes.
+cudaError_t launch_bwd(const BwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t dout_dtype, void* workspace,
+                       cudaStream_t s);
+
 // Tensor maps (2-D TMA descriptors) of one forward call: u, delta, z by rows of the CTA, B and C by the
 // dstate rows of a batch entry.  Passed to the kernel as a __grid_constant__ parameter.
 struct alignas(64) TmaMaps {

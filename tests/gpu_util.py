@@ -152,3 +152,63 @@ def decode_as_sequences(inp, rows):
                 "h0": None if inp.get("h0") is None else np.ascontiguousarray(inp["h0"][b, d]).reshape(1, 1, N)}
         out.append(case)
     return out
+
+
+# Gradients (selscan_bwd): |g - ref| <= a·max|ref| + r·|ref| per tensor, (a, r) by the type the gradient
+# is written in.  fp32 gradients carry the fp32 rounding of sums over up to B·L·N terms (relative 1e-5
+# at these sizes) and the approximate exp2 of the recomputed states; bf16 gradients (du, dδ, dz of bf16
+# inputs) are rounded to 8 significant bits (relative 2^-9) on top.
+GRAD_TOL = {"f32": (1e-4, 1e-4), "bf16": (1e-3, 4e-3)}
+
+
+def gpu_bwd(inp, cot, delta_softplus=True, workspace=None, want_dh0=True):
+    """selscan_bwd on an input dict and a cotangent dict; float64 numpy gradients keyed like
+    oracle.selscan_bwd."""
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    go = to_dev(cot["dout"])
+    gh = to_dev(cot.get("dh_last"))
+    g = ss.selscan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], go, D=t["D"], z=t["z"],
+                       delta_bias=t["delta_bias"], delta_softplus=delta_softplus, h0=t["h0"], dh_last=gh,
+                       workspace=workspace, want_dh0=want_dh0)
+    torch.cuda.synchronize()
+    return {k: (None if v is None else v.float().cpu().numpy().astype(np.float64)) for k, v in g.items()}
+
+
+def oracle_cotangent(cot):
+    """The cotangents as float64 arrays for oracle.selscan_bwd (bf16 bit patterns widened exactly)."""
+    import seeded_inputs as si
+
+    go = cot["dout"]
+    go = si.bf16_bits_to_f32(go) if go.dtype == np.uint16 else go
+    gh = cot.get("dh_last")
+    return go.astype(np.float64), (None if gh is None else gh.astype(np.float64))
+
+
+def check_grads(got, ref, in_dtype, what=""):
+    """Compare every gradient the oracle returns (keys whose oracle value is None are skipped); returns
+    the worst error of each tensor as a fraction of its bound."""
+    worst = {}
+    for key, r in ref.items():
+        if r is None:
+            continue
+        g = got[key]
+        assert g is not None, f"{what} grad {key} missing"
+        assert g.shape == r.shape, f"{what} grad {key} shape {g.shape} != {r.shape}"
+        assert np.isfinite(r).all(), f"{what} grad {key}: the oracle's gradient is not finite (bad test input)"
+        kind = in_dtype if key in ("u", "delta", "z") else "f32"
+        a, rr = GRAD_TOL[kind]
+        scale = float(np.abs(r).max()) if r.size else 0.0
+        err = np.abs(g - r)
+        bound = a * scale + rr * np.abs(r)
+        bad = ~(err <= bound)
+        if bad.any():
+            i = int(np.argmax(np.where(bad, err - bound, -np.inf)))
+            raise AssertionError(f"{what} grad {key}: {int(bad.sum())} of {bad.size} outside tolerance; worst at flat "
+                                 f"{i}: got {g.flat[i]!r} ref {r.flat[i]!r} (bound {bound.flat[i]:.3e}, scale "
+                                 f"{scale:.3e})")
+        worst[key] = float((err / np.maximum(bound, 1e-300)).max()) if r.size else 0.0
+    return worst

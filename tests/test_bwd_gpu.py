@@ -1,0 +1,150 @@
+"""Parity of the backward (selscan_bwd) with the fp64 oracle's gradients, element by element.
+
+The oracle's gradients are pinned against central finite differences of its forward and against the
+adjoint of the materialised causal matrix (tests/oracle_pins.py).  Every case here runs the CUDA
+kernel through the C ABI and compares every gradient tensor: du, dδ, dz, dA, dB, dC, dD, dΔ_bias, dh0.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from gpu_util import check_grads, gpu_bwd, oracle_cotangent, to_dev
+
+pytestmark = pytest.mark.gpu
+
+# (batch, dim, seqlen, dstate, in_dtype, dout_dtype, options)
+CASES = [
+    (2, 40, 100, 16, "f32", "f32", {}),                      # ragged chunk and ragged CTA, every input
+    (2, 64, 128, 16, "bf16", "bf16", {}),                    # whole chunks, vector loads and stores
+    (1, 37, 33, 12, "bf16", "f32", {}),                      # N not a multiple of 4, odd L
+    (3, 33, 47, 1, "f32", "f32", {}),                        # one state
+    (1, 8, 1, 4, "f32", "f32", {}),                          # one step
+    (1, 8, 16, 8, "f32", "bf16", {}),                        # exactly one chunk
+    (1, 70, 260, 16, "f32", "f32", {"has_z": False, "has_D": False, "has_bias": False, "has_h0": False,
+                                    "has_dh_last": False}),  # no optional input
+    (2, 48, 300, 16, "f32", "f32", {"softplus": False}),     # Δ = δ + Δ_bias (no softplus)
+    (2, 96, 2048, 16, "bf16", "bf16", {}),                   # 128 chunks, three CTAs per batch entry
+]
+
+
+def _case(i, B, Dm, L, N, dt, gdt, opt):
+    inp = si.random_case(500 + i, B, Dm, L, N, in_dtype=dt, has_z=opt.get("has_z", True),
+                         has_D=opt.get("has_D", True), has_bias=opt.get("has_bias", True),
+                         has_h0=opt.get("has_h0", True))
+    if not opt.get("softplus", True):
+        # keep Δ = δ + Δ_bias positive without the softplus: δ = |N(0,1)|·0.1, Δ_bias = |Δ_bias|·0.01
+        inp["delta_bias"] = (np.abs(inp["delta_bias"]) * np.float32(0.01)).astype(np.float32)
+        d = inp["delta"]
+        if dt == "bf16":
+            f = si.bf16_bits_to_f32(d)
+            inp["delta"] = si.f32_to_bf16_bits(np.abs(f) * np.float32(0.1))
+        else:
+            inp["delta"] = (np.abs(d) * np.float32(0.1)).astype(np.float32)
+    cot = si.random_cotangents(900 + i, B, Dm, L, N, dout_dtype=gdt, has_dh_last=opt.get("has_dh_last", True))
+    return inp, cot
+
+
+@pytest.mark.parametrize("i", range(len(CASES)))
+def test_bwd_matches_oracle(i):
+    B, Dm, L, N, dt, gdt, opt = CASES[i]
+    inp, cot = _case(i, B, Dm, L, N, dt, gdt, opt)
+    sp = opt.get("softplus", True)
+    got = gpu_bwd(inp, cot, delta_softplus=sp)
+    go, gh = oracle_cotangent(cot)
+    ref = oracle.selscan_bwd(inp, go, gh, delta_softplus=sp)
+    check_grads(got, ref, dt, what=f"case {CASES[i][:6]}")
+
+
+def test_bwd_absent_optional_inputs_give_gradient_at_zero():
+    """dD and dΔ_bias are returned even without D and Δ_bias: they equal the gradients at D = 0 and
+    Δ_bias = 0, which the oracle computes when given explicit zeros."""
+    inp, cot = _case(40, 2, 40, 90, 16, "f32", "f32", {"has_D": False, "has_bias": False})
+    got = gpu_bwd(inp, cot)
+    z = dict(inp)
+    z["D"] = np.zeros(40, np.float32)
+    z["delta_bias"] = np.zeros(40, np.float32)
+    go, gh = oracle_cotangent(cot)
+    ref = oracle.selscan_bwd(z, go, gh)
+    check_grads(got, ref, "f32", what="zero D / bias")
+
+
+def test_bwd_workspace_given_or_pooled():
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    inp, cot = _case(41, 2, 40, 200, 16, "bf16", "f32", {})
+    need = ss.selscan_bwd_workspace_size(2, 40, 200, 16)
+    assert need == 2 * 40 * ((200 + 15) // 16) * 16 * 4
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    a = gpu_bwd(inp, cot, workspace=ws)
+    b = gpu_bwd(inp, cot)
+    go, gh = oracle_cotangent(cot)
+    ref = oracle.selscan_bwd(inp, go, gh)
+    check_grads(a, ref, "bf16", what="given workspace")
+    check_grads(b, ref, "bf16", what="pooled workspace")
+    for k in ("u", "delta", "z", "h0"):  # no atomics in these: identical bits
+        assert np.array_equal(a[k], b[k]), k
+    with pytest.raises(ss.SelscanError) as e:
+        gpu_bwd(inp, cot, workspace=ws[: need - 16])
+    assert e.value.status == 8  # SELSCAN_ERR_SCRATCH
+
+
+def test_bwd_empty_sequence_and_no_rows():
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    inp, cot = _case(42, 2, 8, 0, 4, "f32", "f32", {})
+    got = gpu_bwd(inp, cot)
+    assert got["u"].shape == (2, 8, 0) and got["B"].shape == (2, 4, 0)
+    assert np.all(got["A"] == 0) and np.all(got["D"] == 0) and np.all(got["delta_bias"] == 0)
+    assert np.array_equal(got["h0"], cot["dh_last"].astype(np.float64))  # the state's gradient passes through
+    inp, cot = _case(43, 2, 0, 50, 4, "f32", "f32", {})
+    got = gpu_bwd(inp, cot)
+    assert np.all(got["B"] == 0) and np.all(got["C"] == 0) and got["A"].shape == (0, 4)
+
+def test_bwd_requires_dz_with_z():
+    """The C ABI refuses a call with z but no dz (SELSCAN_ERR_NULL) and enqueues nothing."""
+    import ctypes
+
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    inp, cot = _case(45, 1, 8, 32, 4, "f32", "f32", {})
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A")}
+    go = to_dev(cot["dout"])
+    g = {k: torch.zeros_like(t[k], dtype=torch.float32) for k in ("u", "delta", "A", "B", "C")}
+    lib = ss.load_library()
+    shape = ss.SelscanShape(1, 8, 32, 4, 0, 0)
+    p = lambda x: None if x is None else x.data_ptr()  # noqa: E731
+    st = lib.selscan_bwd(ctypes.byref(shape), p(t["u"]), p(t["delta"]), p(t["A"]), p(t["B"]), p(t["C"]), None,
+                         p(t["z"]), None, 1, None, p(go), None, p(g["u"]), p(g["delta"]), None, p(g["A"]),
+                         p(g["B"]), p(g["C"]), None, None, None, None, 0, None)
+    assert st == 1  # SELSCAN_ERR_NULL
+    assert ss.selscan_last_launch_count() == 0
+
+
+def test_bwd_launches_one_kernel():
+    import selective_state_space_152_b300 as ss
+
+    inp, cot = _case(44, 1, 32, 64, 16, "f32", "f32", {})
+    gpu_bwd(inp, cot)
+    assert ss.selscan_last_launch_count() == 1
+
+
+@pytest.mark.parametrize("name", ["mamba130m_layer", "width_2p8b"])
+def test_bwd_workload_full(name):
+    """Every gradient of a full-size workload against the oracle on all host cores."""
+    w = si.WORKLOADS[name]
+    inp = si.make_inputs(w)
+    B, Dm, L, N = inp["shape"]
+    cot = si.random_cotangents(77, B, Dm, L, N, dout_dtype="bf16")
+    got = gpu_bwd(inp, cot)
+    go, gh = oracle_cotangent(cot)
+    ref = oracle.selscan_bwd(inp, go, gh)
+    check_grads(got, ref, w.in_dtype, what=name)
