@@ -99,6 +99,19 @@ constexpr int kSB = SELSCAN_ROWS_SB;  // steps per sub-block (16 or 32)
 #ifndef SELSCAN_ROWS_DU_SMEM
 #define SELSCAN_ROWS_DU_SMEM 1
 #endif
+// Q > 1: the row's Q partial sums of y meet through a warp buffer (1: each lane writes its partials, then
+// reads the Q partials of the steps it stores) or by recursive halving with shuffles (0).
+#ifndef SELSCAN_ROWS_YRED
+#define SELSCAN_ROWS_YRED 1
+#endif
+// Q > 1: step pairs whose exponentials are formed ahead of the state update in progress.
+#ifndef SELSCAN_ROWS_AHEAD
+#define SELSCAN_ROWS_AHEAD 2
+#endif
+// Pause of the producer warp between polls of its two events, in nanoseconds.
+#ifndef SELSCAN_ROWS_PSLEEP
+#define SELSCAN_ROWS_PSLEEP 64
+#endif
 constexpr int kMaxWarps = 11;  // consumer warps per CTA (one producer warp more): 12 warps, up to 168 registers
 constexpr int kMaxStages = 4;
 
@@ -114,7 +127,12 @@ struct RowsGeom {
   // Warp-private buffer (Q > 1): per row and step pair the record (Δ_t, Δ_t+1, Δu_t, Δu_t+1), plus with ZOH
   // (u_t, u_t+1); rows padded by 16 bytes so that the 8 rows a quarter-warp reads fall in distinct banks.
   static constexpr int REC = (ZOH ? 6 : 4) * (kT / 2) + 4;  // floats per row
-  static constexpr int WARP_FLOATS = (Q > 1 && SELSCAN_ROWS_DU_SMEM) ? RPW * REC : 0;
+  static constexpr int REC_FLOATS = (Q > 1 && SELSCAN_ROWS_DU_SMEM) ? RPW * REC : 0;
+  // y partials (Q > 1, SELSCAN_ROWS_YRED): [q][row][kSB + 4]; the odd number of 16-byte units per row keeps
+  // the 8 lanes of a quarter-warp in distinct banks both when they write and when they read.
+  static constexpr int YS = kSB + 4;
+  static constexpr int Y_FLOATS = (Q > 1 && SELSCAN_ROWS_YRED) ? 32 * YS : 0;
+  static constexpr int WARP_FLOATS = REC_FLOATS + Y_FLOATS;
   static_assert(NS % SPL == 0 && SPL % 4 == 0 && (Q == 1 || Q == 2 || Q == 4), "lanes per row");
   static_assert(RB == 64 || RB == 128, "staged rows of 64 or 128 bytes");
 };
@@ -445,9 +463,11 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         float* tb = tile + static_cast<size_t>(ws) * 2 * kT * TS;
         constexpr int T4 = kT / 4, N4 = NS / 4;
         constexpr int UNITS = (SUMMARY ? 1 : 2) * N4 * T4;
+        // Units with consecutive state quads in a quarter-warp: their 16-byte stores land in distinct banks
+        // (TS = NS + 4 floats per step), where consecutive step quads would collide four ways.
         for (int unit = lane; unit < UNITS; unit += 32) {
-          const int t4 = unit % T4, rest = unit / T4;
-          const int n4 = rest % N4, tt = rest / N4;
+          const int n4 = unit % N4, rest = unit / N4;
+          const int t4 = rest % T4, tt = rest / T4;
           float v[4][4];
 #pragma unroll
           for (int k = 0; k < 4; k++) {
@@ -502,7 +522,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         ok = false;
         break;
       } else {
-        __nanosleep(64);  // neither event yet: leave the issue slots to the consumer warps
+        __nanosleep(SELSCAN_ROWS_PSLEEP);  // neither event yet: leave the issue slots to the consumer warps
       }
     }
     if (!ok && lane == 0) {
@@ -658,12 +678,12 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
       break;
     }
 
-    // 2-3. The scan over the chunk in sub-blocks, then the row's outputs of each sub-block.
+    // 2-3. The scan over the chunk, then the row's outputs of each sub-block.
+    if constexpr (Q == 1) {
 #pragma unroll
-    for (int sbi = 0; sbi < kT / kSB; sbi++) {
-      const int sb = REV ? kT / kSB - 1 - sbi : sbi;
-      float yp[kSB];
-      if constexpr (Q == 1) {
+      for (int sbi = 0; sbi < kT / kSB; sbi++) {
+        const int sb = REV ? kT / kSB - 1 - sbi : sbi;
+        float yp[kSB];
         float xv[kSB], uv[kSB];
         stage_load<Tin, kSB>(xv, st_d, swz, sb * kSB);
         stage_load<Tin, kSB>(uv, st_u, swz, sb * kSB);
@@ -720,91 +740,107 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
           }
           if (row_ok) store_out<kSB>(out, row_off, t0 + sb * kSB, L, vec_out, out_bf16, yp);
         }
-      } else {
-        // Δ and Δu of step t of the sub-block come from the lane that prepared it: lane (t / EPS) of the row
-        // (by shuffles), or from the row's records in the warp buffer.
-        const float4* recs = reinterpret_cast<const float4*>(wrec + r * G::REC);
-        const float2* urec = reinterpret_cast<const float2*>(wrec + r * G::REC + 4 * (kT / 2));
-        auto dpair = [&](int tt) -> float2 {
+      }
+    } else {
+      // Δ and Δu of a step pair come from the lane that prepared them: the row's record of the pair in the
+      // warp buffer (Δ_t, Δ_t+1, Δu_t, Δu_t+1), or shuffles from lane (t / EPS) of the row.
+      constexpr int P = kT / 2, PS = kSB / 2, AH = SELSCAN_ROWS_AHEAD;
+      const float4* recs = reinterpret_cast<const float4*>(wrec + r * G::REC);
+      const float2* urec = reinterpret_cast<const float2*>(wrec + r * G::REC + 4 * (kT / 2));
+      auto record = [&](int gp) -> float4 {
+        if constexpr (SELSCAN_ROWS_DU_SMEM) {
+          return recs[gp];
+        } else {
+          const int tt = 2 * (gp % PS), src = (tt / EPS) * RPW + r, k = (gp / PS) * EPS + tt % EPS;
+          return make_float4(__shfl_sync(kFull, rdl[k], src), __shfl_sync(kFull, rdl[k + 1], src),
+                             __shfl_sync(kFull, rdu[k], src), __shfl_sync(kFull, rdu[k + 1], src));
+        }
+      };
+      // The pairs in scan order g = 0 .. P-1 (pair gp = g, or P-1-g with REV).  The exponentials of pair g
+      // are formed AH pairs ahead of its state update, across sub-block boundaries, so the special-function
+      // unit's latency overlaps the FMAs of the pairs in between (only AH + 1 pairs are live at a time).
+      float4 rq[P];
+      float2 eq[P][SPL], a0q[P][SPL / 2], a1q[P][SPL / 2];
+      auto start = [&](int g) {
+        rq[g] = record(REV ? P - 1 - g : g);
+        expo_pair<SPL>(f2(rq[g].x, rq[g].y), A2d, eq[g], a0q[g], a1q[g]);
+      };
+#pragma unroll
+      for (int g = 0; g < AH && g < P; g++) start(g);
+      float yp[kSB];
+#pragma unroll
+      for (int g = 0; g < P; g++) {
+        if (g + AH < P) start(g + AH);
+        const int gp = REV ? P - 1 - g : g, sb = gp / PS, tt = 2 * (gp % PS);
+        float u0 = 0.f, u1 = 0.f;
+        if (ZOH) {
           if constexpr (SELSCAN_ROWS_DU_SMEM) {
-            return *reinterpret_cast<const float2*>(&recs[(sb * kSB + tt) / 2]);
+            const float2 uu = urec[gp];
+            u0 = uu.x;
+            u1 = uu.y;
           } else {
             const int src = (tt / EPS) * RPW + r, k = sb * EPS + tt % EPS;
-            return f2(__shfl_sync(kFull, rdl[k], src), __shfl_sync(kFull, rdl[k + 1], src));
-          }
-        };
-        // The exponentials of each step pair are formed one pair ahead of its state update, so the
-        // special-function unit's latency overlaps the previous pair's FMAs.
-        float2 e[SPL], a0[SPL / 2], a1[SPL / 2];
-        expo_pair<SPL>(dpair(REV ? kSB - 2 : 0), A2d, e, a0, a1);
-#pragma unroll
-        for (int pi = 0; pi < kSB / 2; pi++) {
-          const int pr = REV ? kSB / 2 - 1 - pi : pi;
-          const int tt = 2 * pr;
-          float2 ne[SPL], na0[SPL / 2], na1[SPL / 2];
-          if (pi + 1 < kSB / 2) expo_pair<SPL>(dpair(REV ? tt - 2 : tt + 2), A2d, ne, na0, na1);
-          float d0, d1, u0 = 0.f, u1 = 0.f;
-          if constexpr (SELSCAN_ROWS_DU_SMEM) {
-            const float4 rc = recs[(sb * kSB + tt) / 2];
-            d0 = rc.z;
-            d1 = rc.w;
-            if (ZOH) {
-              const float2 uu = urec[(sb * kSB + tt) / 2];
-              u0 = uu.x;
-              u1 = uu.y;
-            }
-          } else {
-            const int src = (tt / EPS) * RPW + r, k = sb * EPS + tt % EPS;
-            d0 = __shfl_sync(kFull, rdu[k], src);
-            d1 = __shfl_sync(kFull, rdu[k + 1], src);
-            if (ZOH) {
-              u0 = __shfl_sync(kFull, ru[k], src);
-              u1 = __shfl_sync(kFull, ru[k + 1], src);
-            }
-          }
-          update_pair<SPL, TS, REV, ZOH, SUMMARY>(h, IA, e, a0, a1, f2(d0, d0), f2(d1, d1), f2(u0, u0), f2(u1, u1),
-                                                  tB + (sb * kSB + tt) * TS, tC + (sb * kSB + tt) * TS, yp[tt],
-                                                  yp[tt + 1]);
-          if (pi + 1 < kSB / 2) {
-#pragma unroll
-            for (int n = 0; n < SPL; n++) e[n] = ne[n];
-#pragma unroll
-            for (int q2 = 0; q2 < SPL / 2; q2++) {
-              a0[q2] = na0[q2];
-              a1[q2] = na1[q2];
-            }
+            u0 = __shfl_sync(kFull, ru[k], src);
+            u1 = __shfl_sync(kFull, ru[k + 1], src);
           }
         }
-        if (!SUMMARY) {
-          // The row's Q partial sums of y meet by recursive halving across its lanes: after it, lane q holds
-          // the full y of steps [q·EPS, (q+1)·EPS) of the sub-block, the steps it prepared.
-          if (Q == 4) {
-            halve_partials<kSB, 2 * RPW>(yp, (q & 2) != 0);
-            halve_partials<kSB / 2, RPW>(yp, (q & 1) != 0);
-          } else {
-            halve_partials<kSB, RPW>(yp, (q & 1) != 0);
-          }
-          const int e0 = sb * kSB + q * EPS;  // first output step of this lane, within the chunk
-          float y[EPS];
+        update_pair<SPL, TS, REV, ZOH, SUMMARY>(h, IA, eq[g], a0q[g], a1q[g], f2(rq[g].z, rq[g].z),
+                                                f2(rq[g].w, rq[g].w), f2(u0, u0), f2(u1, u1), tB + 2 * gp * TS,
+                                                tC + 2 * gp * TS, yp[tt], yp[tt + 1]);
+        if (SUMMARY || (g + 1) % PS != 0) continue;
+        // Sub-block sb is complete.  The row's Q partial sums of y meet: after it, lane q holds the full y of
+        // steps [q·EPS, (q+1)·EPS) of the sub-block (the steps it prepared) in yp[0, EPS).
+        if constexpr (SELSCAN_ROWS_YRED) {
+          float* yb = wrec + G::REC_FLOATS;
+          __syncwarp();  // the previous sub-block's partials have been read
+          float4* mine = reinterpret_cast<float4*>(yb + (q * RPW + r) * G::YS);
 #pragma unroll
-          for (int m = 0; m < EPS; m++) y[m] = fmaf(Dd, ru[sb * EPS + m], yp[m]);
-          if (fast && !tail) {  // gate present, fp32 vector stores, live row: no further branches
+          for (int c = 0; c < kSB / 4; c++) mine[c] = make_float4(yp[4 * c], yp[4 * c + 1], yp[4 * c + 2], yp[4 * c + 3]);
+          __syncwarp();
+          float2 acc[EPS / 2];
+#pragma unroll
+          for (int k = 0; k < EPS / 2; k++) acc[k] = f2(0.f, 0.f);
+#pragma unroll
+          for (int qq = 0; qq < Q; qq++) {
+            const float4* src = reinterpret_cast<const float4*>(yb + (qq * RPW + r) * G::YS + q * EPS);
+#pragma unroll
+            for (int c = 0; c < EPS / 4; c++) {
+              const float4 v = src[c];
+              acc[2 * c] = add2s(acc[2 * c], f2(v.x, v.y));
+              acc[2 * c + 1] = add2s(acc[2 * c + 1], f2(v.z, v.w));
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < EPS / 2; k++) {
+            yp[2 * k] = acc[k].x;
+            yp[2 * k + 1] = acc[k].y;
+          }
+        } else if (Q == 4) {
+          halve_partials<kSB, 2 * RPW>(yp, (q & 2) != 0);
+          halve_partials<kSB / 2, RPW>(yp, (q & 1) != 0);
+        } else {
+          halve_partials<kSB, RPW>(yp, (q & 1) != 0);
+        }
+        const int e0 = sb * kSB + q * EPS;  // first output step of this lane, within the chunk
+        float y[EPS];
+#pragma unroll
+        for (int m = 0; m < EPS; m++) y[m] = fmaf(Dd, ru[sb * EPS + m], yp[m]);
+        if (fast && !tail) {  // gate present, fp32 vector stores, live row: no further branches
+          float zv[EPS];
+          stage_load<Tin, EPS>(zv, st_z, swz, e0);
+          float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + row_off + t0 + e0);
+#pragma unroll
+          for (int c = 0; c < EPS / 4; c++)
+            o[c] = make_float4(y[4 * c] * silu_fast(zv[4 * c]), y[4 * c + 1] * silu_fast(zv[4 * c + 1]),
+                               y[4 * c + 2] * silu_fast(zv[4 * c + 2]), y[4 * c + 3] * silu_fast(zv[4 * c + 3]));
+        } else {
+          if (has_z) {
             float zv[EPS];
             stage_load<Tin, EPS>(zv, st_z, swz, e0);
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + row_off + t0 + e0);
 #pragma unroll
-            for (int g = 0; g < EPS / 4; g++)
-              o[g] = make_float4(y[4 * g] * silu_fast(zv[4 * g]), y[4 * g + 1] * silu_fast(zv[4 * g + 1]),
-                                 y[4 * g + 2] * silu_fast(zv[4 * g + 2]), y[4 * g + 3] * silu_fast(zv[4 * g + 3]));
-          } else {
-            if (has_z) {
-              float zv[EPS];
-              stage_load<Tin, EPS>(zv, st_z, swz, e0);
-#pragma unroll
-              for (int m = 0; m < EPS; m++) y[m] *= silu_fast(zv[m]);
-            }
-            if (row_ok) store_out<EPS>(out, row_off, t0 + e0, L, vec_out, out_bf16, y);
+            for (int m = 0; m < EPS; m++) y[m] *= silu_fast(zv[m]);
           }
+          if (row_ok) store_out<EPS>(out, row_off, t0 + e0, L, vec_out, out_bf16, y);
         }
       }
     }
@@ -879,6 +915,7 @@ __global__ void __launch_bounds__(256) selscan_rows_carry_kernel(const FwdParams
 // measured 0.47 on the 65536-step workload).  Used only to rank plans.
 double cost_per_element(int Q) { return Q == 1 ? 0.95 : Q == 2 ? 1.0 : 1.08; }
 constexpr double kSummaryCost = 0.5;
+constexpr double kFullWarps = 10.0;  // consumer warps per SM that keep it busy
 
 struct RowsPlan {
   int warps = 1, stages = 2, nblocks = 1;
@@ -888,9 +925,11 @@ struct RowsPlan {
 
 constexpr int64_t kMinTblock = 256;
 
-// Choose warps per CTA and time blocks: every SM's consumer-warp load (CTAs on the busiest SM times
-// their warps, times rows and steps per warp) over both passes, with a penalty when an SM would hold
-// too few warps to hide latencies.
+// Choose warps per CTA and time blocks by the modelled time of the busiest SM over both passes.  An SM
+// runs its CTAs in rounds of `resident` CTAs (its register, shared-memory and warp limits); a round takes
+// tblock steps of its rows, but a round with fewer than kFullWarps consumer warps cannot hide the
+// special-function and shared-memory latencies and takes as long as one with kFullWarps (measured on
+// B300: 1 CTA of 11 warps per SM beats 2 CTAs of 6 warps whose third CTA runs alone).
 RowsPlan plan_rows(const FwdParams& p, int rpw, int Q, int sms, int max_warps, int per_sm_cap[kMaxWarps + 1]) {
   RowsPlan best;
   const int64_t L = p.seqlen;
@@ -914,11 +953,13 @@ RowsPlan plan_rows(const FwdParams& p, int rpw, int Q, int sms, int max_warps, i
         const int64_t blocks = pass == 0 ? nb : nb - 1;
         const int64_t ctas = cpb * p.batch * blocks;
         const int64_t per_sm = (ctas + sms - 1) / sms;
-        const int64_t resident = per_sm < per_sm_cap[W] ? per_sm : per_sm_cap[W];
-        const double warps_resident = static_cast<double>(resident * W);
-        const double penalty = warps_resident >= 10.0 ? 1.0 : 10.0 / warps_resident;
-        cost += static_cast<double>(per_sm * W) * rpw * static_cast<double>(tb) * cost_per_element(Q) *
-                (pass == 0 ? 1.0 : kSummaryCost) * penalty;
+        const int64_t resident = per_sm_cap[W] > 0 ? per_sm_cap[W] : 1;
+        double warp_rounds = 0.0;  // Σ over rounds of max(consumer warps in the round, kFullWarps)
+        for (int64_t left = per_sm; left > 0; left -= resident) {
+          const double w = static_cast<double>((left < resident ? left : resident) * W);
+          warp_rounds += w > kFullWarps ? w : kFullWarps;
+        }
+        cost += warp_rounds * rpw * static_cast<double>(tb) * cost_per_element(Q) * (pass == 0 ? 1.0 : kSummaryCost);
       }
       if (cost < best.cost * 0.999) {
         best.cost = cost;
