@@ -23,6 +23,8 @@ shard of an N-times-larger batch (weak scaling, no data-path collective).
 sequence and the 2.8B-width layer) the same way, each with its own roofline;
 ``unit_rates`` are the special-function and FMA rates measured on the GPU by the
 library's own probe (selscan_probe_rate), from which the rooflines are derived.
+``backward`` times selscan_bwd (every gradient, bf16 dout) on the same workloads,
+each against the backward's own roofline (``bwd_work``).
 """
 from __future__ import annotations
 
@@ -85,6 +87,25 @@ def fwd_work(batch, dim, seqlen, dstate, in_bytes=2, out_bytes=4, h0=False, h_la
         nbytes += batch * dim * dstate * 4
     return {"elements": elems, "bytes": nbytes, "mufu": elems * (dstate + 4),
             "sfu": {"ex2": elems * (dstate + 2), "lg2": elems, "rcp": elems}, "fp32": elems * (4 * dstate + 8)}
+
+
+def bwd_work(batch, dim, seqlen, dstate, in_bytes=2, dout_bytes=2):
+    """Algorithmic work of one selscan_bwd (gradients of every input of the forward).
+
+    Bytes: u, δ, z, dout read once and du, dδ, dz written once per element; B, C read and dB, dC
+    written once per (b, n, t); A, D, Δ_bias, h0, dh_last, dA, dD, dΔ_bias, dh0 once (the checkpoint
+    workspace is not algorithmic).  Special functions per element: the states recomputed once and
+    undone once (2N exponentials), softplus (an exponential and a logarithm) whose exponential also
+    gives σ(δ + Δ_bias) with one reciprocal, and σ(z) (an exponential and a reciprocal).  FP32: 4 per
+    (element, state) for the recomputation, 9 for the reverse sweep, plus 30 per element.
+    """
+    elems = batch * dim * seqlen
+    bc = batch * dstate * seqlen
+    nbytes = (elems * (6 * in_bytes + dout_bytes) + bc * (2 * in_bytes + 2 * 4) + 2 * dim * dstate * 4
+              + 4 * dim * 4 + 3 * batch * dim * dstate * 4)
+    return {"elements": elems, "bytes": nbytes,
+            "sfu": {"ex2": elems * (2 * dstate + 2), "lg2": elems, "rcp": 2 * elems},
+            "fp32": elems * (13 * dstate + 30)}
 
 
 def step_work(batch, dim, dstate, in_bytes=2, out_bytes=4):
@@ -435,6 +456,8 @@ def run_ours(args, rank, world, local_rank, dist):
         result["decode"] = run_decode(args, torch, ss, device, stream, flush, sms, hbm_gbs)
     if rank == 0 and world == 1 and not args.no_options:
         result["options"] = run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz, rates)
+    if rank == 0 and world == 1 and not args.no_backward:
+        result["backward"] = run_backward(args, torch, ss, device, stream, flush, sms, hbm_gbs, sm_mhz, rates)
     clk.stop()
     result["clocks"] = clk.report()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -585,6 +608,50 @@ def run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm
     return res
 
 
+BACKWARD_WORKLOADS = ("mamba130m_layer", "width_2p8b", "long_seq_65k")
+
+
+def run_backward(args, torch, ss, device, stream, flush, sms, hbm_gbs, sm_mhz, rates):
+    """Secondary: the backward (selscan_bwd, every gradient) on the forward workloads, each call timed after
+    an L2 flush with its workspace allocated beforehand, against the backward's own roofline."""
+    res = {}
+    for name in BACKWARD_WORKLOADS:
+        w = si.WORKLOADS[name]
+        inp = si.make_inputs(w)
+        Bsz, Dm, L, N = inp["shape"]
+        t, _, _ = forward_tensors(torch, inp, w, device)
+        cot = si.random_cotangents(77, Bsz, Dm, L, N, dout_dtype="bf16")
+        go, gh = _dev(torch, cot["dout"], device), _dev(torch, cot["dh_last"], device)
+        ws = torch.empty(ss.selscan_bwd_workspace_size(Bsz, Dm, L, N), dtype=torch.uint8, device=device)
+        g = ss.selscan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], go, D=t["D"], z=t["z"],
+                           delta_bias=t["delta_bias"], h0=t["h0"], dh_last=gh, workspace=ws, stream=stream)
+
+        def call():
+            ss.selscan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], go, D=t["D"], z=t["z"],
+                           delta_bias=t["delta_bias"], h0=t["h0"], dh_last=gh, grads=g, workspace=ws, stream=stream)
+
+        for _ in range(3):
+            flush.zero_()
+            call()
+        launches = ss.selscan_last_launch_count()
+        reps = 5 if L > 10000 else 20
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        secs = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
+        wk = bwd_work(Bsz, Dm, L, N, in_bytes=2 if w.in_dtype == "bf16" else 4, dout_bytes=2)
+        res[name] = {"batch": Bsz, "dim": Dm, "seqlen": L, "dstate": N, "dout_dtype": "bf16",
+                     "us_per_call": secs * 1e6, "elems_per_s": wk["elements"] / secs,
+                     "roofline": roofline_entry(wk, secs, sms, hbm_gbs, sm_mhz, rates=rates),
+                     "launches_per_call": launches, "gpu_launches": launches * reps}
+        del t, g, ws, go, gh
+    return res
+
+
 def run_decode(args, torch, ss, device, stream, flush, sms, hbm_gbs):
     """Secondary: the recurrent decode workload (64 steps of selscan_step carrying the fp32 state)."""
     w = si.WORKLOADS["decode_step"]
@@ -697,6 +764,7 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-options", action="store_true", help="skip the reverse / zero-order-hold timings")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward (selscan_bwd) timings")
     ap.add_argument("--no-sweep", action="store_true", help="skip the other forward workloads")
     ap.add_argument("--sweep-steps", type=int, default=50)
     args = ap.parse_args(argv)

@@ -460,6 +460,7 @@ selscan_status_t selscan_step(const selscan_shape_t* shape, const void* u, const
   p.out = out;
   p.delta_softplus = delta_softplus != 0;
   p.vec_state = (N % 4 == 0) && aligned(state, 16) && aligned(A, 16);
+  p.vec_bc = aligned(B, 4 * ei) && aligned(C, 4 * ei);
   cudaError_t e = selscan::launch_step(p, shape->in_dtype, shape->out_dtype, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
 }

@@ -66,6 +66,7 @@ struct StepParams {
   void* out;
   int delta_softplus;
   int vec_state;  // state / A rows may be accessed as float4 (dstate % 4 == 0, 16-byte aligned)
+  int vec_bc;     // B, C rows may be read four states at a time (bases aligned to 4 elements)
 };
 
 cudaError_t launch_fwd(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype, cudaStream_t s);

@@ -4,20 +4,18 @@
 //   y = Σ_n C[b,n] h[n] + D[d] u,  out = y silu(z)
 // This is the recurrent (RNN-mode) form of the selective scan with a constant-size state
 // ("Mamba架构深度剖析：如何以线性时间重塑序列建模" §3; recurrence from "Mamba状态空间模型深度解析"
-// §2.1).  It is a streaming read-modify-write of the fp32 state [B, D, N]: Q = NS/4 consecutive
-// threads share one row, each owning four states (one 16-byte vector), so a warp reads and writes
-// 512 contiguous bytes of state per access.  The Q partial sums of y meet with shuffles.
+// §2.1).  It is a streaming read-modify-write of the fp32 state [B, D, N].  For 16 aligned states and
+// D >= 64, four threads per row with B and C staged per CTA (selscan_step_quad_kernel); otherwise
+// Q = NS/4 consecutive threads per row, each owning four states (one 16-byte vector), the Q partial
+// sums of y meeting with shuffles.  A one-thread-per-row kernel stays selectable for comparison.
+#include <climits>
+#include <cstdlib>
+
 #include "selscan_internal.cuh"
 
 namespace selscan {
 namespace {
 
-// The one-thread-per-row kernel below serves 16 vector-aligned states (measured 49 us per step
-// against 60 us for the quarter-row kernel on 256 x 5120 rows, L2 flushed before each step);
-// SELSCAN_STEP_ROW=0 at build time keeps the quarter-row kernel for every dstate.
-#ifndef SELSCAN_STEP_ROW
-#define SELSCAN_STEP_ROW 1
-#endif
 #ifndef SELSCAN_STEP_ROW_MINB
 #define SELSCAN_STEP_ROW_MINB 4
 #endif
@@ -142,10 +140,75 @@ __global__ void __launch_bounds__(256, SELSCAN_STEP_ROW_MINB) selscan_step_row16
   static_cast<Tout*>(p.out)[row] = from_f32<Tout>(y);
 }
 
+// Four threads per row for 16 aligned states, one 16-byte state quad each: a warp reads and writes 512
+// contiguous bytes of state per instruction (measured on B300: an 84 MB in-place update in this layout
+// reaches 0.79 of the copy bandwidth, one thread per row 0.70).  Each thread reads its four B and C values
+// itself (8 or 16 bytes each, shared by every row of the batch entry and so served by L1), and forms Δ and
+// the gate itself: no barrier and no value crossing lanes before the y reduction, so every load of a
+// thread is in flight at once.
+template <typename Tin>
+__device__ __forceinline__ float4 load_quad(const Tin* p) {
+  if constexpr (sizeof(Tin) == 2) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
+                       __uint_as_float(w.y & 0xffff0000u));
+  } else {
+    return __ldg(reinterpret_cast<const float4*>(p));
+  }
+}
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256) selscan_step_quad_kernel(const StepParams p) {
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  const int64_t rows = p.batch * p.dim;
+  const int64_t row = gid >> 2;
+  const int q = threadIdx.x & 3;
+  if (row >= rows) return;  // whole rows leave together (4 divides the warp)
+  int64_t b;
+  if (rows <= INT32_MAX) {  // 32-bit division where the row index fits
+    b = static_cast<uint32_t>(row) / static_cast<uint32_t>(p.dim);
+  } else {
+    b = row / p.dim;
+  }
+  const int64_t d = row - b * p.dim;
+  float4 h = __ldcs(reinterpret_cast<const float4*>(p.state + row * 16) + q);
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p.A + d * 16) + q);
+  const float4 bv = load_quad(static_cast<const Tin*>(p.B) + b * 16 + 4 * q);
+  const float4 cv = load_quad(static_cast<const Tin*>(p.C) + b * 16 + 4 * q);
+  const float uu = to_f32(static_cast<const Tin*>(p.u)[row]);
+  const float x = to_f32(static_cast<const Tin*>(p.delta)[row]) + (p.delta_bias ? p.delta_bias[d] : 0.f);
+  const float zz = p.z ? to_f32(static_cast<const Tin*>(p.z)[row]) : 0.f;
+  const float Dd = p.D ? p.D[d] : 0.f;
+  const float dt = p.delta_softplus ? softplus_fast(x) : x;
+  const float dtl = dt * kLog2e, du = dt * uu;
+  h.x = fmaf(ex2_approx(dtl * a.x), h.x, du * bv.x);
+  h.y = fmaf(ex2_approx(dtl * a.y), h.y, du * bv.y);
+  h.z = fmaf(ex2_approx(dtl * a.z), h.z, du * bv.z);
+  h.w = fmaf(ex2_approx(dtl * a.w), h.w, du * bv.w);
+  __stcs(reinterpret_cast<float4*>(p.state + row * 16) + q, h);
+  float y = fmaf(cv.x, h.x, fmaf(cv.y, h.y, fmaf(cv.z, h.z, cv.w * h.w)));
+  y += __shfl_xor_sync(kFull, y, 1);
+  y += __shfl_xor_sync(kFull, y, 2);
+  if (q == 0) {
+    y = fmaf(Dd, uu, y);
+    if (p.z) y *= silu_fast(zz);
+    static_cast<Tout*>(p.out)[row] = from_f32<Tout>(y);
+  }
+}
+
 template <int NS, typename Tin, typename Tout>
 cudaError_t launch_ns(const StepParams& p, cudaStream_t s) {
+  // SELSCAN_STEP: "quad", "row" or "generic" (default: the first that applies).
+  const char* force = getenv("SELSCAN_STEP");
+  const char f = force ? force[0] : 'q';
+  if (f == 'q' && NS == 16 && p.dstate == 16 && p.vec_state && p.vec_bc) {
+    const int64_t rows = p.batch * p.dim;
+    selscan_step_quad_kernel<Tin, Tout><<<static_cast<unsigned>((rows + 63) / 64), 256, 0, s>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+  }
   // (With at least 256 channels a CTA's 256 rows span at most two batch entries.)
-  if (SELSCAN_STEP_ROW && NS == 16 && p.dstate == 16 && p.vec_state && p.dim >= 256) {
+  if (f != 'g' && NS == 16 && p.dstate == 16 && p.vec_state && p.dim >= 256) {
     const int64_t rows = p.batch * p.dim;
     selscan_step_row16_kernel<Tin, Tout><<<static_cast<unsigned>((rows + 255) / 256), 256, 0, s>>>(p);
     count_launches(1);

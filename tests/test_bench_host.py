@@ -23,6 +23,20 @@ def test_fwd_work_counts_the_bench_workload():
     assert w["sfu"] == {"ex2": elems * 18, "lg2": elems, "rcp": elems}
 
 
+def test_bwd_work_counts_the_backward_of_the_bench_workload():
+    # 8 x 1536 x 2048 x 16, bf16 inputs and dout; gradients du, dδ, dz in bf16, dB, dC fp32
+    w = bench.bwd_work(8, 1536, 2048, 16, in_bytes=2, dout_bytes=2)
+    elems = 8 * 1536 * 2048
+    per_elem = 3 * 2 + 2 + 3 * 2               # u, δ, z, dout read; du, dδ, dz written
+    bc = 8 * 16 * 2048 * (2 * 2 + 2 * 4)       # B, C read (bf16); dB, dC written (fp32)
+    small = 2 * 1536 * 16 * 4 + 4 * 1536 * 4  # A, dA; D, Δ_bias, dD, dΔ_bias
+    states = 3 * 8 * 1536 * 16 * 4             # h0, dh_last, dh0
+    assert w["bytes"] == elems * per_elem + bc + small + states
+    assert w["sfu"] == {"ex2": elems * 34, "lg2": elems, "rcp": 2 * elems}
+    t = bench.roofline_times(w, sms=148, hbm_gbs=6493.4, sm_mhz=2032.0)
+    assert t["mufu"] > t["hbm"]  # the backward is bound by its exponentials, as the forward is
+
+
 def test_step_work_counts_the_decode_workload():
     w = bench.step_work(256, 5120, 16)
     rows = 256 * 5120

@@ -387,6 +387,38 @@ def test_step_rows_spanning_batch_entries(dt):
     check_h(state.cpu().numpy().astype(np.float64), href, what="decode state")
 
 
+STEP_CASES = [(5, 100, 4, "bf16", True), (5, 192, 4, "f32", False), (1400, 256, 3, "bf16", True)]
+
+
+@pytest.mark.parametrize("kern", ["quad", "row", "generic"])
+@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: "x".join(map(str, c[:3])) + f"-{c[3]}-z{int(c[4])}")
+def test_step_kernels(case, kern, monkeypatch):
+    """Each decode kernel, a few steps carrying the state, against the forward oracle (D = 100 puts a
+    batch-entry boundary inside CTAs of the quad kernel, whose 64 rows then span two entries)."""
+    import torch
+
+    import selective_state_space_152_b300 as ss
+
+    monkeypatch.setenv("SELSCAN_STEP", kern)
+    Bsz, Dm, T, dt, has_z = case
+    inp = si.random_case(137 + Bsz, Bsz, Dm, T, 16, in_dtype=dt, has_z=has_z)
+    ref, href = oracle.selscan_fwd(inp)
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    state = t["h0"].clone()
+    outs = []
+    for s in range(T):
+        z = None if t["z"] is None else t["z"][..., s].contiguous()
+        outs.append(ss.selscan_step(t["u"][..., s].contiguous(), t["delta"][..., s].contiguous(), t["A"],
+                                    t["B"][..., s].contiguous(), t["C"][..., s].contiguous(), state, D=t["D"],
+                                    z=z, delta_bias=t["delta_bias"]))
+        assert ss.selscan_last_launch_count() == 1
+    torch.cuda.synchronize()
+    got = torch.stack(outs, dim=-1).cpu().numpy().astype(np.float64)
+    check_out(got, ref, dt, what=f"decode {kern}")
+    check_h(state.cpu().numpy().astype(np.float64), href, what=f"decode {kern} state")
+    assert ss.selscan_device_status() == 0
+
+
 def test_step_small_fp32_odd_dstate():
     import torch
 
