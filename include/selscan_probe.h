@@ -43,6 +43,19 @@ typedef enum {
 
 selscan_status_t selscan_probe_rate(int unit, double* per_clk_per_sm);
 
+/*
+ * The bounded wait of the forward kernels, made to run out on purpose, so that a caller (or a test) can
+ * check on a real GPU that a lost asynchronous copy ends in an error status rather than a hang.  One CTA
+ * of 32 threads waits on an mbarrier phase whose one arrival announces 16 bytes that no copy delivers
+ * (no copy is issued: nothing is in flight when the waits end).  Each thread polls the phase with the
+ * same helper the forward kernels use, at most `polls` times (1 .. 2^20; the kernels themselves use
+ * 2^18, about one second at the 3.9 us a poll of an incomplete phase suspends on B300), then gives up: it sets the device status word that selscan_device_status() reads (which then
+ * returns 1 until reset) and returns.  *completed receives the number of waits that saw the phase
+ * complete (0 when the bound works).  Synchronous; allocates one int with cudaMalloc for the call.
+ * Returns SELSCAN_ERR_NULL, SELSCAN_ERR_SHAPE (polls out of range) or SELSCAN_ERR_CUDA.
+ */
+selscan_status_t selscan_probe_wait_timeout(int64_t polls, int* completed);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,7 @@ STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SE
           8: "SELSCAN_ERR_SCRATCH"}
 EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
             "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_probe_rate",
-            "selscan_last_launch_count", "selscan_bwd", "selscan_bwd_workspace_size")
+            "selscan_last_launch_count", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_probe_wait_timeout")
 # Units of selscan_probe_rate (include/selscan_probe.h).
 PROBE_UNITS = {"ex2": 0, "lg2": 1, "rcp": 2, "tanh": 3, "ffma": 4, "ffma2": 5}
 SELSCAN_FLAG_REVERSE, SELSCAN_FLAG_ZOH = 1, 2
@@ -82,6 +82,8 @@ def load_library(path: Optional[str] = None):
     lib.selscan_bwd.restype = i32
     lib.selscan_bwd_workspace_size.argtypes = [shp]
     lib.selscan_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.selscan_probe_wait_timeout.argtypes = [ctypes.c_int64, ctypes.POINTER(ctypes.c_int)]
+    lib.selscan_probe_wait_timeout.restype = i32
     lib.selscan_probe_rate.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
     lib.selscan_probe_rate.restype = i32
     if path is None:
@@ -120,6 +122,14 @@ def selscan_probe_rate(unit: str) -> float:
     r = ctypes.c_double(0.0)
     _check(load_library().selscan_probe_rate(PROBE_UNITS[unit], ctypes.byref(r)))
     return r.value
+
+
+def selscan_probe_wait_timeout(polls: int = 4096) -> int:
+    """Run the forward kernels' bounded wait on a phase that never completes (see include/selscan_probe.h);
+    returns the number of waits that completed (0 when the bound works).  Synchronous."""
+    c = ctypes.c_int(-1)
+    _check(load_library().selscan_probe_wait_timeout(int(polls), ctypes.byref(c)))
+    return c.value
 
 
 def _check(status: int):
@@ -383,7 +393,7 @@ def selscan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, delta_
     return g
 
 
-__all__ = ["selscan_fwd", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step",
+__all__ = ["selscan_fwd", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_probe_wait_timeout", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step",
            "selscan_status_string", "selscan_abi_version", "selscan_last_cuda_error", "selscan_device_status",
            "selscan_probe_rate", "selscan_last_launch_count", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED",
            "PROBE_UNITS"]

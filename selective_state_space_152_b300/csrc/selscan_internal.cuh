@@ -152,6 +152,9 @@ void count_launches(int n);
 cudaError_t read_device_error(int* value, int reset);
 cudaError_t read_seq_device_error(int* value, int reset);
 cudaError_t read_rows_device_error(int* value, int reset);
+// Launch the bounded-wait probe (one CTA waiting on a phase that never completes, each wait giving up
+// after `polls` polls) and synchronise; *completed = waits that saw the phase complete.
+cudaError_t probe_wait_timeout(long long polls, int* completed);
 
 // Where the time-block scratch of a forward call comes from: the CUDA memory pool of the call's stream
 // (cudaMallocAsync / cudaFreeAsync), or the library's fixed device array (selscan_fwd_noalloc).
@@ -211,7 +214,13 @@ __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.f + __
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr long long kWaitLimit = 1ll << 26;  // polls of an mbarrier before a copy is declared lost
+// Polls of an mbarrier phase before a copy is declared lost.  Each mbarrier.try_wait that finds the phase
+// incomplete suspends the thread for about 3.9 us on B300 (measured with selscan_probe_wait_timeout), so
+// 2^18 polls give up after about one second, far beyond any copy's latency.
+constexpr long long kWaitLimit = 1ll << 18;
+// Idle rounds of a producer warp (a non-blocking test of its events and a 64 ns pause each, about
+// 0.2 us) before it declares its pipeline stuck: also about one second.
+constexpr long long kIdleLimit = 1ll << 22;
 
 __device__ __forceinline__ float lg2_approx(float x) {
   float r;

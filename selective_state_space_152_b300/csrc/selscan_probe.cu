@@ -125,3 +125,11 @@ extern "C" selscan_status_t selscan_probe_rate(int unit, double* per_clk_per_sm)
   *per_clk_per_sm = med > 0 ? ops / med : 0.0;
   return SELSCAN_OK;
 }
+
+// The bounded wait of the forward kernels, made to run out: see include/selscan_probe.h.
+extern "C" selscan_status_t selscan_probe_wait_timeout(int64_t polls, int* completed) {
+  if (!completed) return SELSCAN_ERR_NULL;
+  if (polls < 1 || polls > (int64_t{1} << 20)) return SELSCAN_ERR_SHAPE;
+  const cudaError_t e = selscan::probe_wait_timeout(static_cast<long long>(polls), completed);
+  return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
+}

@@ -228,8 +228,9 @@ __device__ __forceinline__ void store_out(void* __restrict__ out, int64_t row_of
 
 // Bounded wait on an mbarrier phase that also gives up when another warp of the CTA has raised the
 // abort flag (checked every 256 polls).
-__device__ __noinline__ bool wait_or_abort_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  for (long long i = 0; i < kWaitLimit; i++) {
+__device__ __noinline__ bool wait_or_abort_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                long long limit = kWaitLimit) {
+  for (long long i = 0; i < limit; i++) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255) == 255 && *abort_flag) return false;
   }
@@ -516,8 +517,8 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
       __syncwarp();
       if (progress) {
         idle = 0;
-      } else if (++idle > kWaitLimit / 16 || ((idle & 255) == 255 && *abort_flag)) {
-        if (idle > kWaitLimit / 16) atomicExch(&g_selscan_rows_error, 1);
+      } else if (++idle > kIdleLimit || ((idle & 255) == 255 && *abort_flag)) {
+        if (idle > kIdleLimit) atomicExch(&g_selscan_rows_error, 1);
         *abort_flag = 1;
         ok = false;
         break;
@@ -1193,6 +1194,41 @@ cudaError_t launch_fwd_rows(const FwdParams& p_in, selscan_dtype_t in_dtype, sel
   cudaError_t e = in_dtype == SELSCAN_F32 ? dispatch_rows_opts<float>(p, o, s, &tb)
                                           : dispatch_rows_opts<__nv_bfloat16>(p, o, s, &tb);
   if (too_big) *too_big = tb;
+  return e;
+}
+
+namespace {
+
+// One CTA whose threads wait, with the bounded wait of the forward kernels, on an mbarrier phase that
+// expects 16 bytes no copy will deliver (no copy is issued, so none is in flight when the waits give up).
+__global__ void __launch_bounds__(32) selscan_wait_probe_kernel(long long polls, int* completed) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_abort;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_expect_tx(&bar, 16);  // the phase's one arrival, with 16 bytes still to come
+  __syncthreads();
+  if (wait_or_abort_slow(&bar, 0, &s_abort, polls)) atomicAdd(completed, 1);
+}
+
+}  // namespace
+
+cudaError_t probe_wait_timeout(long long polls, int* completed) {
+  int* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, sizeof(int));
+  if (e != cudaSuccess) return e;
+  e = cudaMemset(d, 0, sizeof(int));
+  if (e == cudaSuccess) {
+    selscan_wait_probe_kernel<<<1, 32>>>(polls, d);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(completed, d, sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFree(d);
   return e;
 }
 
