@@ -411,8 +411,8 @@ selscan_status_t selscan_bwd(const selscan_shape_t* shape, const void* u, const 
   p.ddelta_bias = ddelta_bias;
   p.dh0 = dh0;
   p.delta_softplus = delta_softplus != 0;
-  p.vec_in = aligned(u, 16) && aligned(delta, 16) && (!z || aligned(z, 16)) && L % (16 / ei) == 0;
-  p.vec_dout = aligned(dout, 16) && L % (16 / eo) == 0;
+  p.vec_in = aligned(u, 4 * ei) && aligned(delta, 4 * ei) && (!z || aligned(z, 4 * ei)) && L % 4 == 0;
+  p.vec_dout = aligned(dout, 4 * eo) && L % 4 == 0;
   p.vec_grad = aligned(du, 4 * ei) && aligned(ddelta, 4 * ei) && (!dz || aligned(dz, 4 * ei)) && L % 4 == 0;
   p.vec_dbc = aligned(dB, 16) && aligned(dC, 16) && L % 4 == 0;
   e = selscan::launch_bwd(p, shape->in_dtype, shape->out_dtype, workspace, s);

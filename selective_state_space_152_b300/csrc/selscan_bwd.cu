@@ -16,13 +16,17 @@
 // sweeps it backwards.
 //
 // Decomposition: a CTA owns kRows channels of one batch entry; 4 lanes share a row, lane q owning
-// states [4q, 4q+4) (lane = 8q + r), so the 8 rows of a warp that read one state group read the same
-// B, C values (shared-memory broadcast).  The row's lanes add their partial sums (y, Σ G B, Σ A G Ā h)
-// with two shuffles.  dB and dC are sums over the channels of a batch entry: per step a warp adds up
-// its 8 rows' contributions by recursive halving (7 shuffles leave lane 8q + r holding the sum of value
-// r of {dB of states 4q..4q+3, dC of states 4q..4q+3}), the CTA adds its warps in shared memory at the
-// end of the chunk, and one 16-byte atomic add per (tensor, state, 4 steps) goes to global memory.  dA,
-// dD and dΔ_bias are summed per lane in registers over the sequence and added with one atomic per row.
+// states [4q, 4q+4) as two float2 pairs (packed fp32x2 arithmetic), lane = 8q + r, so the 8 rows of a
+// warp that read one state group read the same B, C values (shared-memory broadcast).  Lane q also owns
+// steps [4q, 4q+4) of every chunk: it loads their inputs, forms Δ, Δu, σ(x), σ(z) and dy once, hands
+// Δ, Δu and dy to the row's other lanes by shuffles, and stores those steps' du, dδ and dz.  The next
+// chunk's inputs are loaded into registers while the current one is computed.  The row's lanes add
+// their partial sums over states (y, Σ G B, Σ A G Ā h) with two shuffles.  dB and dC are sums over the
+// channels of a batch entry: per step a warp adds up its 8 rows' contributions by recursive halving (7
+// shuffles leave lane 8q + r holding the sum of value r of {dB of states 4q..4q+3, dC of states
+// 4q..4q+3}), the CTA adds its warps in shared memory at the end of the chunk, and one 16-byte atomic add
+// per (tensor, state, 4 steps) goes to global memory.  dA, dD and dΔ_bias are summed in registers over
+// the sequence and added with one atomic per row and value.
 #include "selscan_internal.cuh"
 
 namespace selscan {
@@ -32,9 +36,11 @@ constexpr int kBT = 16;         // steps per chunk (checkpoint interval)
 constexpr int kBW = 4;          // warps per CTA
 constexpr int kRows = kBW * 8;  // channels per CTA
 constexpr int kNS = 16;         // states per row held by the 4 lanes (lanes mask states >= N)
+constexpr int kThreads = kBW * 32;
+constexpr int kTS = kNS + 4;  // floats per step of the B, C tile: the stagers' column writes spread over banks
 
 struct BwdSmem {
-  float bc[2][kBT][kNS];     // B, C of the chunk, [step][state]
+  float bc[2][kBT][kTS];     // B, C of the chunk, [step][state]
   float h[kBW][kBT][32][4];  // per warp: h_{t-1} of every step of the chunk, per lane
   float red[kBW][kBT][32];   // per warp and step: the 8-row sums of dB, dC (lane 8q + r: value r)
 };
@@ -60,37 +66,53 @@ __device__ __forceinline__ void softplus_sigmoid(float x, float& sp, float& sg) 
   sg = (x >= 0.f ? 1.f : e) * rcp_approx(1.f + e);
 }
 
-// Up to kBT consecutive values of one row as fp32: 16-byte vector loads when the chunk is whole and the
-// row is aligned, else element by element (zeros past len).
+// The raw bits of a lane's four steps of one row: 8 bytes of bf16 or 16 bytes of fp32.
 template <typename T>
-__device__ __forceinline__ void load_chunk(const T* __restrict__ src, int len, bool vec, float (&v)[kBT]) {
-  if (vec && len == kBT) {
+struct Quad {
+  uint32_t w[sizeof(T)];  // 2 words (bf16) or 4 words (fp32)
+};
+
+// Load steps [t, t + n) of a row (n = 0..4; zeros past n): one 8- or 16-byte load when all four exist
+// and the row is aligned for it.
+template <typename T>
+__device__ __forceinline__ Quad<T> load_quad(const T* __restrict__ src, int n, bool vec) {
+  Quad<T> qd;
+  if (vec && n == 4) {
     if constexpr (sizeof(T) == 2) {
-      const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-      for (int j = 0; j < kBT / 8; j++) {
-        const uint4 w = __ldg(s + j);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          v[8 * j + 2 * k] = __uint_as_float(ws[k] << 16);
-          v[8 * j + 2 * k + 1] = __uint_as_float(ws[k] & 0xffff0000u);
-        }
-      }
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+      qd.w[0] = v.x;
+      qd.w[1] = v.y;
     } else {
-      const float4* s = reinterpret_cast<const float4*>(src);
-#pragma unroll
-      for (int j = 0; j < kBT / 4; j++) {
-        const float4 w = __ldg(s + j);
-        v[4 * j] = w.x;
-        v[4 * j + 1] = w.y;
-        v[4 * j + 2] = w.z;
-        v[4 * j + 3] = w.w;
-      }
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+      qd.w[0] = v.x;
+      qd.w[1] = v.y;
+      qd.w[2] = v.z;
+      qd.w[3] = v.w;
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < kBT; i++) v[i] = i < len ? to_f32(src[i]) : 0.f;
+    for (int k = 0; k < static_cast<int>(sizeof(T)); k++) qd.w[k] = 0u;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      if (k >= n) break;
+      if constexpr (sizeof(T) == 2) {
+        const uint32_t b = __bfloat16_as_ushort(src[k]);
+        qd.w[k >> 1] |= (k & 1) ? (b << 16) : b;
+      } else {
+        qd.w[k] = __float_as_uint(src[k]);
+      }
+    }
+  }
+  return qd;
+}
+
+template <typename T>
+__device__ __forceinline__ float quad_at(const Quad<T>& qd, int k) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t w = qd.w[k >> 1];
+    return __uint_as_float((k & 1) ? (w & 0xffff0000u) : (w << 16));
+  } else {
+    return __uint_as_float(qd.w[k]);
   }
 }
 
@@ -111,35 +133,53 @@ __device__ __forceinline__ void store4(T* dst, int n, bool vec, const float (&v)
   }
 }
 
-// B (ntensors = 1) or B and C (2) of steps [t0, t0 + len) of batch entry b as [step][state], zeros past
-// N and past len.
-template <typename Tin>
-__device__ __forceinline__ void stage_bc(BwdSmem& sm, const BwdParams& p, int64_t b, int64_t t0, int len,
-                                         int ntensors) {
-  const Tin* Bp = static_cast<const Tin*>(p.B);
-  const Tin* Cp = static_cast<const Tin*>(p.C);
-  for (int i = threadIdx.x; i < ntensors * kBT * kNS; i += kBW * 32) {
-    const int tensor = i / (kBT * kNS), rest = i % (kBT * kNS), n = rest / kBT, tt = rest % kBT;
-    float v = 0.f;
-    if (n < p.dstate && tt < len) v = to_f32((tensor ? Cp : Bp)[(b * p.dstate + n) * p.seqlen + t0 + tt]);
-    sm.bc[tensor][tt][n] = v;
-  }
-}
-
-// Keep `v` (the value of step i of the chunk, equal on the row's 4 lanes) in the slot of the lane q that
-// stores steps [4q, 4q + 4).
-__device__ __forceinline__ void keep_slot(float (&slot)[4], int i, int q, float v) {
-  if ((i >> 2) == q) slot[i & 3] = v;
-}
-
 // Values of step quad q of a chunk of len steps that exist (0..4).
 __device__ __forceinline__ int quad_len(int len, int q) {
   const int n = len - 4 * q;
   return n < 0 ? 0 : (n > 4 ? 4 : n);
 }
 
+// Steps in chunk c of a sequence of L steps.
+__device__ __forceinline__ int chunk_len(int64_t L, int c) {
+  const int64_t left = L - static_cast<int64_t>(c) * kBT;
+  return static_cast<int>(left < kBT ? left : kBT);
+}
+
+// The B (and C) values of a chunk that thread tid stages: element e = tid + kThreads·j of the
+// [tensor][state][step] chunk, j = 0, 1 for B and 2, 3 for C.  Zero past N and past the chunk.
+template <typename Tin, int NT>
+struct BCStage {
+  float v[2 * NT];
+  __device__ __forceinline__ void load(const BwdParams& p, int64_t b, int c) {
+    const int len = chunk_len(p.seqlen, c);
+    const int64_t t0 = static_cast<int64_t>(c) * kBT;
+#pragma unroll
+    for (int j = 0; j < 2 * NT; j++) {
+      const int e = static_cast<int>(threadIdx.x) + kThreads * j;
+      const int tensor = e / (kBT * kNS), n = (e / kBT) % kNS, tt = e % kBT;
+      float x = 0.f;
+      if (n < p.dstate && tt < len)
+        x = to_f32(static_cast<const Tin*>(tensor ? p.C : p.B)[(b * p.dstate + n) * p.seqlen + t0 + tt]);
+      v[j] = x;
+    }
+  }
+  __device__ __forceinline__ void store(BwdSmem& sm) const {
+#pragma unroll
+    for (int j = 0; j < 2 * NT; j++) {
+      const int e = static_cast<int>(threadIdx.x) + kThreads * j;
+      sm.bc[e / (kBT * kNS)][e % kBT][(e / kBT) % kNS] = v[j];
+    }
+  }
+};
+static_assert(2 * kThreads == kBT * kNS, "two B values and two C values per thread and chunk");
+
+// Broadcast step i's value from the lane of the row that prepared it (lane 8·(i / 4) + r).
+__device__ __forceinline__ float from_prep(const float (&v)[4], int i, int r) {
+  return __shfl_sync(kFull, v[i & 3], (i >> 2) * 8 + r);
+}
+
 template <typename Tin, typename Tg>
-__global__ void __launch_bounds__(kBW * 32, 3) selscan_bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -154,140 +194,191 @@ __global__ void __launch_bounds__(kBW * 32, 3) selscan_bwd_kernel(const BwdParam
   const int nchunks = static_cast<int>((L + kBT - 1) / kBT);
   const float bias = p.delta_bias ? p.delta_bias[dd] : 0.f;
   const float Dd = p.D ? p.D[dd] : 0.f;
-  const Tin* u_row = static_cast<const Tin*>(p.u) + grow * L;
-  const Tin* x_row = static_cast<const Tin*>(p.delta) + grow * L;
-  const Tin* z_row = p.z ? static_cast<const Tin*>(p.z) + grow * L : nullptr;
-  const Tg* go_row = static_cast<const Tg*>(p.dout) + grow * L;
-  float A2[4], Araw[4], h[4];
+  const bool softplus = p.delta_softplus != 0;
+  const Tin* u_row = static_cast<const Tin*>(p.u) + grow * L + 4 * q;
+  const Tin* x_row = static_cast<const Tin*>(p.delta) + grow * L + 4 * q;
+  const Tin* z_row = p.z ? static_cast<const Tin*>(p.z) + grow * L + 4 * q : nullptr;
+  const Tg* go_row = static_cast<const Tg*>(p.dout) + grow * L + 4 * q;
+  // This lane's states as pairs: A·log2 e (exponent), A (dΔ), h.
+  float2 A2[2], Ar[2], h[2];
 #pragma unroll
-  for (int k = 0; k < 4; k++) {
-    const int n = 4 * q + k;
-    Araw[k] = n < N ? p.A[dd * N + n] : 0.f;
-    A2[k] = Araw[k] * kLog2e;
-    h[k] = (n < N && row_ok && p.h0) ? p.h0[grow * N + n] : 0.f;
+  for (int k = 0; k < 2; k++) {
+    const int n = 4 * q + 2 * k;
+    const float a0 = n < N ? p.A[dd * N + n] : 0.f, a1 = n + 1 < N ? p.A[dd * N + n + 1] : 0.f;
+    Ar[k] = f2(a0, a1);
+    A2[k] = f2(a0 * kLog2e, a1 * kLog2e);
+    const bool has = row_ok && p.h0;
+    h[k] = f2(has && n < N ? p.h0[grow * N + n] : 0.f, has && n + 1 < N ? p.h0[grow * N + n + 1] : 0.f);
   }
   float4* ck = reinterpret_cast<float4*>(p.ckpt) + grow * nchunks * (kNS / 4) + q;
 
   // ---- phase 1: the forward, keeping the state at the start of every chunk --------------------------
-  for (int c = 0; c < nchunks; c++) {
-    const int64_t t0 = static_cast<int64_t>(c) * kBT;
-    const int len = static_cast<int>(L - t0 < kBT ? L - t0 : kBT);
-    __syncthreads();  // the previous chunk's B has been read
-    stage_bc<Tin>(sm, p, b, t0, len, 1);
-    if (row_ok) ck[static_cast<int64_t>(c) * (kNS / 4)] = make_float4(h[0], h[1], h[2], h[3]);
-    float uv[kBT], xv[kBT];
-    load_chunk(u_row + t0, len, p.vec_in, uv);
-    load_chunk(x_row + t0, len, p.vec_in, xv);
-    __syncthreads();
+  {
+    BCStage<Tin, 1> bs;
+    bs.load(p, b, 0);
+    Quad<Tin> uq = load_quad(u_row, quad_len(chunk_len(L, 0), q), p.vec_in);
+    Quad<Tin> xq = load_quad(x_row, quad_len(chunk_len(L, 0), q), p.vec_in);
+    for (int c = 0; c < nchunks; c++) {
+      const int len = chunk_len(L, c);
+      __syncthreads();  // the previous chunk's B has been read
+      bs.store(sm);
+      if (row_ok) ck[static_cast<int64_t>(c) * (kNS / 4)] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+      // This lane's steps: Δ and Δu (zero past the chunk: an identity step).
+      float dlq[4], duq[4];
 #pragma unroll
-    for (int i = 0; i < kBT; i++) {
-      if (i >= len) break;
-      const float x = xv[i] + bias;
-      const float dl = p.delta_softplus ? softplus_fast(x) : x;
-      const float du = dl * uv[i];
-      const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
-      const float Bk[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
+      for (int m = 0; m < 4; m++) {
+        const float x = quad_at(xq, m) + bias;
+        const float dl = softplus ? softplus_fast(x) : x;
+        const bool in = 4 * q + m < len;
+        dlq[m] = in ? dl : 0.f;
+        duq[m] = in ? dl * quad_at(uq, m) : 0.f;
+      }
+      if (c + 1 < nchunks) {  // the next chunk's inputs, in flight during this one
+        const int nlen = chunk_len(L, c + 1);
+        bs.load(p, b, c + 1);
+        uq = load_quad(u_row + (c + 1) * kBT, quad_len(nlen, q), p.vec_in);
+        xq = load_quad(x_row + (c + 1) * kBT, quad_len(nlen, q), p.vec_in);
+      }
+      __syncthreads();
 #pragma unroll
-      for (int k = 0; k < 4; k++) h[k] = fmaf(ex2_approx(dl * A2[k]), h[k], du * Bk[k]);
+      for (int i = 0; i < kBT; i++) {
+        if (i >= len) break;
+        const float dl = from_prep(dlq, i, r), du = from_prep(duq, i, r);
+        const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
+        const float2 d2 = f2(dl, dl), du2 = f2(du, du);
+        const float2 e0 = mul2s(d2, A2[0]), e1 = mul2s(d2, A2[1]);
+        const float2 a0 = f2(ex2_approx(e0.x), ex2_approx(e0.y)), a1 = f2(ex2_approx(e1.x), ex2_approx(e1.y));
+        h[0] = fma2s(a0, h[0], mul2s(du2, f2(Bv.x, Bv.y)));
+        h[1] = fma2s(a1, h[1], mul2s(du2, f2(Bv.z, Bv.w)));
+      }
     }
   }
 
   // ---- phase 2: the chunks from last to first ----------------------------------------------------------
-  float g[4], dA[4] = {0.f, 0.f, 0.f, 0.f};
+  float2 g[2], dA[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
-  for (int k = 0; k < 4; k++) {
-    const int n = 4 * q + k;
-    g[k] = (n < N && row_ok && p.dh_last) ? p.dh_last[grow * N + n] : 0.f;
+  for (int k = 0; k < 2; k++) {
+    const int n = 4 * q + 2 * k;
+    const bool has = row_ok && p.dh_last;
+    g[k] = f2(has && n < N ? p.dh_last[grow * N + n] : 0.f, has && n + 1 < N ? p.dh_last[grow * N + n + 1] : 0.f);
   }
-  float dD = 0.f, dbias = 0.f;
+  float dD = 0.f, dbias = 0.f;  // over this lane's steps
   const bool has_z = p.z != nullptr;
+  const bool b2 = r & 4, b1 = r & 2, b0 = r & 1;
+  BCStage<Tin, 2> bs;
+  bs.load(p, b, nchunks - 1);
+  Quad<Tin> uq, xq, zq;
+  Quad<Tg> gq;
+  {
+    const int n0 = quad_len(chunk_len(L, nchunks - 1), q);
+    const int64_t o = static_cast<int64_t>(nchunks - 1) * kBT;
+    uq = load_quad(u_row + o, n0, p.vec_in);
+    xq = load_quad(x_row + o, n0, p.vec_in);
+    if (has_z) zq = load_quad(z_row + o, n0, p.vec_in);
+    gq = load_quad(go_row + o, n0, p.vec_dout);
+  }
   for (int c = nchunks - 1; c >= 0; c--) {
     const int64_t t0 = static_cast<int64_t>(c) * kBT;
-    const int len = static_cast<int>(L - t0 < kBT ? L - t0 : kBT);
+    const int len = chunk_len(L, c);
+    const int nq = quad_len(len, q);
     __syncthreads();  // the previous chunk's B, C and dB/dC sums have been read
-    stage_bc<Tin>(sm, p, b, t0, len, 2);
+    bs.store(sm);
     // (Rows past D have no checkpoints: channel 0's belong to its own row.  Their dout is 0, so every
     // contribution they make is 0 whatever their states are.)
     const float4 c4 = row_ok ? ck[static_cast<int64_t>(c) * (kNS / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
-    float hc[4] = {c4.x, c4.y, c4.z, c4.w};
-    float uv[kBT], dlv[kBT], dyv[kBT], sgv[kBT];
-    {
-      float xv[kBT], gov[kBT], zv[kBT];
-      load_chunk(u_row + t0, len, p.vec_in, uv);
-      load_chunk(x_row + t0, len, p.vec_in, xv);
-      load_chunk(go_row + t0, len, p.vec_dout, gov);
-      if (has_z) load_chunk(z_row + t0, len, p.vec_in, zv);
-      if (!row_ok) {
+    float2 hc[2] = {f2(c4.x, c4.y), f2(c4.z, c4.w)};
+    // This lane's steps: Δ, Δu, σ(x), dy and the factor of y in dz (zero past the chunk).
+    float dlq[4], duq[4], sgq[4], dyq[4], fzq[4], uqv[4];
 #pragma unroll
-        for (int i = 0; i < kBT; i++) gov[i] = 0.f;
+    for (int m = 0; m < 4; m++) {
+      const bool in = m < nq;
+      const float x = quad_at(xq, m) + bias, uu = quad_at(uq, m);
+      float dl = x, sg = 1.f;
+      if (softplus) softplus_sigmoid(x, dl, sg);
+      const float go = row_ok ? quad_at(gq, m) : 0.f;
+      float dy = go, fz = 0.f;
+      if (has_z) {
+        const float zz = quad_at(zq, m);
+        const float sz = rcp_approx(1.f + ex2_approx(-zz * kLog2e));
+        dy = go * zz * sz;
+        fz = go * sz * fmaf(zz, 1.f - sz, 1.f);
       }
-      __syncthreads();
-      // Rerun the chunk from its checkpoint: h_{t-1} of every step to shared memory, y, dy and dz.
-      float dzs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < kBT; i++) {
-        if (i >= len) {
-          uv[i] = dlv[i] = dyv[i] = sgv[i] = 0.f;
-          continue;
-        }
-        const float x = xv[i] + bias;
-        float dl = x, sg = 1.f;
-        if (p.delta_softplus) softplus_sigmoid(x, dl, sg);
-        *reinterpret_cast<float4*>(sm.h[warp][i][lane]) = make_float4(hc[0], hc[1], hc[2], hc[3]);
-        const float du = dl * uv[i];
-        const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
-        const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
-        const float Bk[4] = {Bv.x, Bv.y, Bv.z, Bv.w}, Ck[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
-        float yp = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          hc[k] = fmaf(ex2_approx(dl * A2[k]), hc[k], du * Bk[k]);
-          yp = fmaf(Ck[k], hc[k], yp);
-        }
-        float dy = gov[i];
-        if (has_z) {
-          const float y = fmaf(Dd, uv[i], row_sum(yp));
-          const float zz = zv[i];
-          const float sz = rcp_approx(1.f + ex2_approx(-zz * kLog2e));
-          dy = gov[i] * zz * sz;
-          keep_slot(dzs, i, q, gov[i] * y * sz * fmaf(zz, 1.f - sz, 1.f));
-        }
-        dlv[i] = dl;
-        dyv[i] = dy;
-        sgv[i] = sg;
-      }
-      const int nq = quad_len(len, q);
-      if (has_z && row_ok && nq > 0) store4(static_cast<Tin*>(p.dz) + grow * L + t0 + 4 * q, nq, p.vec_grad, dzs);
+      dlq[m] = in ? dl : 0.f;
+      duq[m] = in ? dl * uu : 0.f;
+      sgq[m] = sg;
+      dyq[m] = in ? dy : 0.f;
+      fzq[m] = fz;
+      uqv[m] = uu;
     }
+    if (c > 0) {  // the next chunk (in scan order: the previous one in time), in flight during this one
+      const int n1 = quad_len(chunk_len(L, c - 1), q);
+      const int64_t o = static_cast<int64_t>(c - 1) * kBT;
+      bs.load(p, b, c - 1);
+      uq = load_quad(u_row + o, n1, p.vec_in);
+      xq = load_quad(x_row + o, n1, p.vec_in);
+      if (has_z) zq = load_quad(z_row + o, n1, p.vec_in);
+      gq = load_quad(go_row + o, n1, p.vec_dout);
+    }
+    __syncthreads();
+    // Rerun the chunk from its checkpoint: h_{t-1} of every step to shared memory, y for dz.
+    float dlv[kBT], duv[kBT], dyv[kBT], dzs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kBT; i++) {
+      if (i >= len) {
+        dlv[i] = duv[i] = dyv[i] = 0.f;
+        continue;
+      }
+      const float dl = from_prep(dlq, i, r), du = from_prep(duq, i, r);
+      dlv[i] = dl;
+      duv[i] = du;
+      dyv[i] = from_prep(dyq, i, r);
+      *reinterpret_cast<float4*>(sm.h[warp][i][lane]) = make_float4(hc[0].x, hc[0].y, hc[1].x, hc[1].y);
+      const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
+      const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
+      const float2 d2 = f2(dl, dl), du2 = f2(du, du);
+      const float2 e0 = mul2s(d2, A2[0]), e1 = mul2s(d2, A2[1]);
+      const float2 a0 = f2(ex2_approx(e0.x), ex2_approx(e0.y)), a1 = f2(ex2_approx(e1.x), ex2_approx(e1.y));
+      hc[0] = fma2s(a0, hc[0], mul2s(du2, f2(Bv.x, Bv.y)));
+      hc[1] = fma2s(a1, hc[1], mul2s(du2, f2(Bv.z, Bv.w)));
+      if (has_z) {
+        const float2 yp2 = fma2s(f2(Cv.z, Cv.w), hc[1], mul2s(f2(Cv.x, Cv.y), hc[0]));
+        const float y = row_sum(yp2.x + yp2.y);
+        if ((i >> 2) == q) dzs[i & 3] = fmaf(Dd, uqv[i & 3], y) * fzq[i & 3];
+      }
+    }
+    if (has_z && row_ok && nq > 0) store4(static_cast<Tin*>(p.dz) + grow * L + t0 + 4 * q, nq, p.vec_grad, dzs);
     __syncwarp();
     // The reverse sweep of the chunk; hn holds h_t (the state after the step being undone).
-    float hn[4] = {hc[0], hc[1], hc[2], hc[3]};
+    float2 hn[2] = {hc[0], hc[1]};
     float dus[4] = {0.f, 0.f, 0.f, 0.f}, dxs[4] = {0.f, 0.f, 0.f, 0.f};
-    const bool b2 = r & 4, b1 = r & 2, b0 = r & 1;
 #pragma unroll
     for (int i = kBT - 1; i >= 0; i--) {
       if (i >= len) continue;
       const float4 hp4 = *reinterpret_cast<const float4*>(sm.h[warp][i][lane]);
-      const float hp[4] = {hp4.x, hp4.y, hp4.z, hp4.w};
       const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
       const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
-      const float Bk[4] = {Bv.x, Bv.y, Bv.z, Bv.w}, Ck[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
-      const float dl = dlv[i], uu = uv[i], dy = dyv[i], dlu = dl * uu;
-      float sGB = 0.f, sAGw = 0.f, v[8];
+      const float2 hp[2] = {f2(hp4.x, hp4.y), f2(hp4.z, hp4.w)};
+      const float2 B2[2] = {f2(Bv.x, Bv.y), f2(Bv.z, Bv.w)}, C2[2] = {f2(Cv.x, Cv.y), f2(Cv.z, Cv.w)};
+      const float dl = dlv[i], dy = dyv[i];
+      const float2 d2 = f2(dl, dl), dy2 = f2(dy, dy), du2 = f2(duv[i], duv[i]);
+      float2 sGB = f2(0.f, 0.f), sAGw = f2(0.f, 0.f), vB[2], vC[2];
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        const float ab = ex2_approx(dl * A2[k]);
-        const float G = fmaf(dy, Ck[k], g[k]);
-        const float t = G * (ab * hp[k]);  // G Ā h_{t-1}
-        v[k] = G * dlu;                    // this row's dB
-        v[4 + k] = dy * hn[k];             // this row's dC
-        sGB = fmaf(G, Bk[k], sGB);
-        sAGw = fmaf(Araw[k], t, sAGw);
-        dA[k] = fmaf(t, dl, dA[k]);
-        g[k] = G * ab;
+      for (int k = 0; k < 2; k++) {
+        const float2 e = mul2s(d2, A2[k]);
+        const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
+        const float2 G = fma2s(dy2, C2[k], g[k]);
+        const float2 t = mul2s(G, mul2s(ab, hp[k]));  // G Ā h_{t-1}
+        vB[k] = mul2s(G, du2);                        // this row's dB
+        vC[k] = mul2s(dy2, hn[k]);                    // this row's dC
+        sGB = fma2s(G, B2[k], sGB);
+        sAGw = fma2s(Ar[k], t, sAGw);
+        dA[k] = fma2s(t, d2, dA[k]);
+        g[k] = mul2s(G, ab);
         hn[k] = hp[k];
       }
-      // dB, dC: the sum over the warp's 8 rows by recursive halving; lane 8q + r ends with value r.
+      // dB, dC: the sum over the warp's 8 rows by recursive halving; lane 8q + r ends with value r of
+      // {dB of states 4q..4q+3, dC of states 4q..4q+3}.
+      const float v[8] = {vB[0].x, vB[0].y, vB[1].x, vB[1].y, vC[0].x, vC[0].y, vC[1].x, vC[1].y};
       float w4[4], w2[2];
 #pragma unroll
       for (int j = 0; j < 4; j++) {
@@ -300,15 +391,16 @@ __global__ void __launch_bounds__(kBW * 32, 3) selscan_bwd_kernel(const BwdParam
         w2[j] = (b1 ? w4[2 + j] : w4[j]) + __shfl_xor_sync(kFull, send, 2);
       }
       sm.red[warp][i][lane] = (b0 ? w2[1] : w2[0]) + __shfl_xor_sync(kFull, b0 ? w2[0] : w2[1], 1);
-      const float S = row_sum(sGB), T = row_sum(sAGw);
-      const float du = fmaf(dy, Dd, dl * S);
-      const float dx = fmaf(uu, S, T) * sgv[i];
-      keep_slot(dus, i, q, du);
-      keep_slot(dxs, i, q, dx);
-      dD = fmaf(dy, uu, dD);
-      dbias += dx;
+      const float S = row_sum(sGB.x + sGB.y), T = row_sum(sAGw.x + sAGw.y);
+      if ((i >> 2) == q) {  // the lane that prepared this step stores its gradients
+        const int m = i & 3;
+        const float dx = fmaf(uqv[m], S, T) * sgq[m];
+        dus[m] = fmaf(dy, Dd, dl * S);
+        dxs[m] = dx;
+        dD = fmaf(dy, uqv[m], dD);
+        dbias += dx;
+      }
     }
-    const int nq = quad_len(len, q);
     if (row_ok && nq > 0) {
       store4(static_cast<Tin*>(p.du) + grow * L + t0 + 4 * q, nq, p.vec_grad, dus);
       store4(static_cast<Tin*>(p.ddelta) + grow * L + t0 + 4 * q, nq, p.vec_grad, dxs);
@@ -337,13 +429,20 @@ __global__ void __launch_bounds__(kBW * 32, 3) selscan_bwd_kernel(const BwdParam
       }
     }
   }
+  dD = row_sum(dD);
+  dbias = row_sum(dbias);
   if (!row_ok) return;
 #pragma unroll
-  for (int k = 0; k < 4; k++) {
-    const int n = 4 * q + k;
-    if (n >= N) continue;
-    if (p.dh0) p.dh0[grow * N + n] = g[k];
-    atomicAdd(p.dA + dd * N + n, dA[k]);
+  for (int k = 0; k < 2; k++) {
+    const int n = 4 * q + 2 * k;
+    if (n < N) {
+      if (p.dh0) p.dh0[grow * N + n] = g[k].x;
+      atomicAdd(p.dA + dd * N + n, dA[k].x);
+    }
+    if (n + 1 < N) {
+      if (p.dh0) p.dh0[grow * N + n + 1] = g[k].y;
+      atomicAdd(p.dA + dd * N + n + 1, dA[k].y);
+    }
   }
   if (q == 0) {
     if (p.dD) atomicAdd(p.dD + dd, dD);
@@ -351,7 +450,7 @@ __global__ void __launch_bounds__(kBW * 32, 3) selscan_bwd_kernel(const BwdParam
   }
 }
 
-static_assert(kBW * 32 == 2 * kNS * kBT / 4, "one thread per (tensor, state, step quad) of a chunk");
+static_assert(kThreads == 2 * kNS * kBT / 4, "one thread per (tensor, state, step quad) of a chunk");
 
 template <typename Tin, typename Tg>
 cudaError_t launch_typed(const BwdParams& p, cudaStream_t s) {
@@ -360,7 +459,7 @@ cudaError_t launch_typed(const BwdParams& p, cudaStream_t s) {
   cudaError_t e =
       cudaFuncSetAttribute(selscan_bwd_kernel<Tin, Tg>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  selscan_bwd_kernel<Tin, Tg><<<grid, kBW * 32, smem, s>>>(p);
+  selscan_bwd_kernel<Tin, Tg><<<grid, kThreads, smem, s>>>(p);
   count_launches(1);
   return cudaGetLastError();
 }

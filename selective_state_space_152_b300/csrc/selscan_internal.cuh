@@ -97,8 +97,8 @@ struct BwdParams {
   float* dh0;          // nullable
   float* ckpt;         // workspace: the state at the start of every chunk, [rows][chunks][16]
   int delta_softplus;
-  int vec_in;    // u, delta, z rows may be read with 16-byte vectors
-  int vec_dout;  // dout rows may be read with 16-byte vectors
+  int vec_in;    // u, delta, z may be read four steps at a time (8- or 16-byte loads)
+  int vec_dout;  // dout may be read four steps at a time
   int vec_grad;  // du, ddelta, dz may be written four steps at a time (8- or 16-byte stores)
   int vec_dbc;   // dB, dC may take 16-byte atomic adds
 };
