@@ -325,7 +325,7 @@ size_t selscan_bwd_workspace_size(const selscan_shape_t* shape) {
   int64_t rows, elems;
   if (!mul_ok(shape->batch, shape->dim, &rows) || !mul_ok(rows, shape->seqlen, &elems) || elems > INT64_MAX / 16)
     return 0;
-  return selscan::bwd_workspace_bytes(rows, shape->seqlen);
+  return selscan::bwd_workspace_bytes(shape->batch, shape->dim, shape->seqlen);
 }
 
 // The backward: the checks of the forward's inputs plus dout, dh_last and the gradient outputs, zeroing
@@ -350,7 +350,7 @@ selscan_status_t selscan_bwd(const selscan_shape_t* shape, const void* u, const 
   if (elems > INT64_MAX / 16 || bc_elems > INT64_MAX / 4 || states > INT64_MAX / 4) return SELSCAN_ERR_SHAPE;
   if (Bsz > 65535) return SELSCAN_ERR_UNSUPPORTED;  // one grid row per batch entry
   const size_t ei = dsize(shape->in_dtype), eo = dsize(shape->out_dtype);
-  const size_t ws_need = selscan::bwd_workspace_bytes(rows, L);
+  const size_t ws_need = selscan::bwd_workspace_bytes(Bsz, Dm, L);
   if (workspace && workspace_bytes < ws_need) return SELSCAN_ERR_SCRATCH;
   const Span ins[] = {{u, elems * (int64_t)ei},    {delta, elems * (int64_t)ei}, {A, an * 4},
                       {B, bc_elems * (int64_t)ei}, {C, bc_elems * (int64_t)ei},  {D, Dm * 4},

@@ -27,6 +27,8 @@
 // 4q..4q+3}), the CTA adds its warps in shared memory at the end of the chunk, and one 16-byte atomic add
 // per (tensor, state, 4 steps) goes to global memory.  dA, dD and dΔ_bias are summed in registers over
 // the sequence and added with one atomic per row and value.
+#include <cstdlib>
+
 #include "selscan_internal.cuh"
 
 namespace selscan {
@@ -192,6 +194,11 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
   const int64_t L = p.seqlen;
   const int N = p.dstate;
   const int nchunks = static_cast<int>((L + kBT - 1) / kBT);
+  // This CTA's time block: chunks [cb, ce).
+  const int kb = blockIdx.z;
+  const int cpb = static_cast<int>(p.tblock / kBT);
+  const int cb = kb * cpb, ce = cb + cpb < nchunks ? cb + cpb : nchunks;
+  const int64_t rows = p.batch * p.dim;
   const float bias = p.delta_bias ? p.delta_bias[dd] : 0.f;
   const float Dd = p.D ? p.D[dd] : 0.f;
   const bool softplus = p.delta_softplus != 0;
@@ -199,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
   const Tin* x_row = static_cast<const Tin*>(p.delta) + grow * L + 4 * q;
   const Tin* z_row = p.z ? static_cast<const Tin*>(p.z) + grow * L + 4 * q : nullptr;
   const Tg* go_row = static_cast<const Tg*>(p.dout) + grow * L + 4 * q;
+  // The block's start state: h0 for one block, else the carried start state.
+  const float* hs = p.nblocks > 1 ? p.hstart + (static_cast<int64_t>(kb) * rows + grow) * kNS : nullptr;
   // This lane's states as pairs: A·log2 e (exponent), A (dΔ), h.
   float2 A2[2], Ar[2], h[2];
 #pragma unroll
@@ -207,18 +216,23 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
     const float a0 = n < N ? p.A[dd * N + n] : 0.f, a1 = n + 1 < N ? p.A[dd * N + n + 1] : 0.f;
     Ar[k] = f2(a0, a1);
     A2[k] = f2(a0 * kLog2e, a1 * kLog2e);
-    const bool has = row_ok && p.h0;
-    h[k] = f2(has && n < N ? p.h0[grow * N + n] : 0.f, has && n + 1 < N ? p.h0[grow * N + n + 1] : 0.f);
+    if (hs) {
+      h[k] = f2(row_ok && n < N ? hs[n] : 0.f, row_ok && n + 1 < N ? hs[n + 1] : 0.f);
+    } else {
+      const bool has = row_ok && p.h0;
+      h[k] = f2(has && n < N ? p.h0[grow * N + n] : 0.f, has && n + 1 < N ? p.h0[grow * N + n + 1] : 0.f);
+    }
   }
   float4* ck = reinterpret_cast<float4*>(p.ckpt) + grow * nchunks * (kNS / 4) + q;
 
   // ---- phase 1: the forward, keeping the state at the start of every chunk --------------------------
   {
     BCStage<Tin, 1> bs;
-    bs.load(p, b, 0);
-    Quad<Tin> uq = load_quad(u_row, quad_len(chunk_len(L, 0), q), p.vec_in);
-    Quad<Tin> xq = load_quad(x_row, quad_len(chunk_len(L, 0), q), p.vec_in);
-    for (int c = 0; c < nchunks; c++) {
+    bs.load(p, b, cb);
+    const int64_t o0 = static_cast<int64_t>(cb) * kBT;
+    Quad<Tin> uq = load_quad(u_row + o0, quad_len(chunk_len(L, cb), q), p.vec_in);
+    Quad<Tin> xq = load_quad(x_row + o0, quad_len(chunk_len(L, cb), q), p.vec_in);
+    for (int c = cb; c < ce; c++) {
       const int len = chunk_len(L, c);
       __syncthreads();  // the previous chunk's B has been read
       bs.store(sm);
@@ -233,11 +247,11 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
         dlq[m] = in ? dl : 0.f;
         duq[m] = in ? dl * quad_at(uq, m) : 0.f;
       }
-      if (c + 1 < nchunks) {  // the next chunk's inputs, in flight during this one
+      if (c + 1 < ce) {  // the next chunk's inputs, in flight during this one
         const int nlen = chunk_len(L, c + 1);
         bs.load(p, b, c + 1);
-        uq = load_quad(u_row + (c + 1) * kBT, quad_len(nlen, q), p.vec_in);
-        xq = load_quad(x_row + (c + 1) * kBT, quad_len(nlen, q), p.vec_in);
+        uq = load_quad(u_row + static_cast<int64_t>(c + 1) * kBT, quad_len(nlen, q), p.vec_in);
+        xq = load_quad(x_row + static_cast<int64_t>(c + 1) * kBT, quad_len(nlen, q), p.vec_in);
       }
       __syncthreads();
 #pragma unroll
@@ -255,29 +269,35 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
   }
 
   // ---- phase 2: the chunks from last to first ----------------------------------------------------------
+  // The gradient with respect to the block's end state: dh_last for one block, else the carried one.
+  const float* ge = p.nblocks > 1 ? p.gend + (static_cast<int64_t>(kb) * rows + grow) * kNS : nullptr;
   float2 g[2], dA[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
   for (int k = 0; k < 2; k++) {
     const int n = 4 * q + 2 * k;
-    const bool has = row_ok && p.dh_last;
-    g[k] = f2(has && n < N ? p.dh_last[grow * N + n] : 0.f, has && n + 1 < N ? p.dh_last[grow * N + n + 1] : 0.f);
+    if (ge) {
+      g[k] = f2(row_ok && n < N ? ge[n] : 0.f, row_ok && n + 1 < N ? ge[n + 1] : 0.f);
+    } else {
+      const bool has = row_ok && p.dh_last;
+      g[k] = f2(has && n < N ? p.dh_last[grow * N + n] : 0.f, has && n + 1 < N ? p.dh_last[grow * N + n + 1] : 0.f);
+    }
   }
   float dD = 0.f, dbias = 0.f;  // over this lane's steps
   const bool has_z = p.z != nullptr;
   const bool b2 = r & 4, b1 = r & 2, b0 = r & 1;
   BCStage<Tin, 2> bs;
-  bs.load(p, b, nchunks - 1);
+  bs.load(p, b, ce - 1);
   Quad<Tin> uq, xq, zq;
   Quad<Tg> gq;
   {
-    const int n0 = quad_len(chunk_len(L, nchunks - 1), q);
-    const int64_t o = static_cast<int64_t>(nchunks - 1) * kBT;
+    const int n0 = quad_len(chunk_len(L, ce - 1), q);
+    const int64_t o = static_cast<int64_t>(ce - 1) * kBT;
     uq = load_quad(u_row + o, n0, p.vec_in);
     xq = load_quad(x_row + o, n0, p.vec_in);
     if (has_z) zq = load_quad(z_row + o, n0, p.vec_in);
     gq = load_quad(go_row + o, n0, p.vec_dout);
   }
-  for (int c = nchunks - 1; c >= 0; c--) {
+  for (int c = ce - 1; c >= cb; c--) {
     const int64_t t0 = static_cast<int64_t>(c) * kBT;
     const int len = chunk_len(L, c);
     const int nq = quad_len(len, q);
@@ -310,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
       fzq[m] = fz;
       uqv[m] = uu;
     }
-    if (c > 0) {  // the next chunk (in scan order: the previous one in time), in flight during this one
+    if (c > cb) {  // the next chunk (in scan order: the previous one in time), in flight during this one
       const int n1 = quad_len(chunk_len(L, c - 1), q);
       const int64_t o = static_cast<int64_t>(c - 1) * kBT;
       bs.load(p, b, c - 1);
@@ -435,12 +455,13 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
 #pragma unroll
   for (int k = 0; k < 2; k++) {
     const int n = 4 * q + 2 * k;
+    const bool first = kb == 0;  // the block whose start is h0
     if (n < N) {
-      if (p.dh0) p.dh0[grow * N + n] = g[k].x;
+      if (p.dh0 && first) p.dh0[grow * N + n] = g[k].x;
       atomicAdd(p.dA + dd * N + n, dA[k].x);
     }
     if (n + 1 < N) {
-      if (p.dh0) p.dh0[grow * N + n + 1] = g[k].y;
+      if (p.dh0 && first) p.dh0[grow * N + n + 1] = g[k].y;
       atomicAdd(p.dA + dd * N + n + 1, dA[k].y);
     }
   }
@@ -452,13 +473,198 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
 
 static_assert(kThreads == 2 * kNS * kBT / 4, "one thread per (tensor, state, step quad) of a chunk");
 
+// Summaries of the time blocks (every block computes both; the carries leave the first block's f and
+// the last block's e unused).  Over block kb, from a zero start, in one forward sweep:
+//   e = the end state (h_t = Ā_t h_{t-1} + Δ_t u_t B_t from h = 0),
+//   f = Σ_t (Π_{s ≤ r ≤ t} Ā_r) dy_t C_t, the gradient with respect to the state before the block that
+//       the block's dy contributes when the gradient after it is 0 (g ← (g + dy_t C_t) Ā_t undone from
+//       the block's end),
+//   ΣΔ, whose 2^(A·log2e·ΣΔ) is the product of the block's Ā (it carries h forward and g backward).
+template <typename Tin, typename Tg>
+__global__ void __launch_bounds__(kThreads) selscan_bwd_summary_kernel(const BwdParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane & 7, q = lane >> 3;
+  const int64_t b = blockIdx.y;
+  const int64_t d = static_cast<int64_t>(blockIdx.x) * kRows + warp * 8 + r;
+  const bool row_ok = d < p.dim;
+  const int64_t dd = row_ok ? d : 0;
+  const int64_t grow = b * p.dim + dd;
+  const int64_t L = p.seqlen;
+  const int N = p.dstate;
+  const int nchunks = static_cast<int>((L + kBT - 1) / kBT);
+  const int kb = blockIdx.z;
+  const int cpb = static_cast<int>(p.tblock / kBT);
+  const int cb = kb * cpb, ce = cb + cpb < nchunks ? cb + cpb : nchunks;
+  const float bias = p.delta_bias ? p.delta_bias[dd] : 0.f;
+  const bool softplus = p.delta_softplus != 0, has_z = p.z != nullptr;
+  const Tin* u_row = static_cast<const Tin*>(p.u) + grow * L + 4 * q;
+  const Tin* x_row = static_cast<const Tin*>(p.delta) + grow * L + 4 * q;
+  const Tin* z_row = has_z ? static_cast<const Tin*>(p.z) + grow * L + 4 * q : nullptr;
+  const Tg* go_row = static_cast<const Tg*>(p.dout) + grow * L + 4 * q;
+  float2 A2[2], e[2], P[2], f[2];
+#pragma unroll
+  for (int k = 0; k < 2; k++) {
+    const int n = 4 * q + 2 * k;
+    A2[k] = f2(n < N ? p.A[dd * N + n] * kLog2e : 0.f, n + 1 < N ? p.A[dd * N + n + 1] * kLog2e : 0.f);
+    e[k] = f2(0.f, 0.f);
+    P[k] = f2(1.f, 1.f);
+    f[k] = f2(0.f, 0.f);
+  }
+  float sumD = 0.f;  // over this lane's steps
+  BCStage<Tin, 2> bs;
+  bs.load(p, b, cb);
+  Quad<Tin> uq, xq, zq;
+  Quad<Tg> gq;
+  auto load_inputs = [&](int c) {
+    const int n = quad_len(chunk_len(L, c), q);
+    const int64_t o = static_cast<int64_t>(c) * kBT;
+    uq = load_quad(u_row + o, n, p.vec_in);
+    xq = load_quad(x_row + o, n, p.vec_in);
+    if (has_z) zq = load_quad(z_row + o, n, p.vec_in);
+    gq = load_quad(go_row + o, n, p.vec_dout);
+  };
+  load_inputs(cb);
+  for (int c = cb; c < ce; c++) {
+    const int len = chunk_len(L, c);
+    const int nq = quad_len(len, q);
+    __syncthreads();
+    bs.store(sm);
+    float dlq[4], duq[4], dyq[4];
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+      const bool in = m < nq;
+      const float x = quad_at(xq, m) + bias;
+      const float dl = softplus ? softplus_fast(x) : x;
+      const float go = row_ok ? quad_at(gq, m) : 0.f;
+      float dy = go;
+      if (has_z) {
+        const float zz = quad_at(zq, m);
+        dy = go * zz * rcp_approx(1.f + ex2_approx(-zz * kLog2e));
+      }
+      dlq[m] = in ? dl : 0.f;
+      duq[m] = in ? dl * quad_at(uq, m) : 0.f;
+      dyq[m] = in ? dy : 0.f;
+      sumD += dlq[m];
+    }
+    if (c + 1 < ce) {
+      bs.load(p, b, c + 1);
+      load_inputs(c + 1);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kBT; i++) {
+      if (i >= len) break;
+      const float dl = from_prep(dlq, i, r), du = from_prep(duq, i, r), dy = from_prep(dyq, i, r);
+      const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
+      const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
+      const float2 d2 = f2(dl, dl), du2 = f2(du, du), dy2 = f2(dy, dy);
+      const float2 B2[2] = {f2(Bv.x, Bv.y), f2(Bv.z, Bv.w)}, C2[2] = {f2(Cv.x, Cv.y), f2(Cv.z, Cv.w)};
+#pragma unroll
+      for (int k = 0; k < 2; k++) {
+        const float2 x2 = mul2s(d2, A2[k]);
+        const float2 a = f2(ex2_approx(x2.x), ex2_approx(x2.y));
+        e[k] = fma2s(a, e[k], mul2s(du2, B2[k]));
+        P[k] = mul2s(P[k], a);
+        f[k] = fma2s(P[k], mul2s(dy2, C2[k]), f[k]);
+      }
+    }
+  }
+  sumD = row_sum(sumD);
+  if (!row_ok) return;
+  const int64_t rows = p.batch * p.dim;
+  float* o = p.summ + (static_cast<int64_t>(kb) * rows + grow) * (2 * kNS) + 4 * q;
+  *reinterpret_cast<float4*>(o) = make_float4(e[0].x, e[0].y, e[1].x, e[1].y);
+  *reinterpret_cast<float4*>(o + kNS) = make_float4(f[0].x, f[0].y, f[1].x, f[1].y);
+  if (q == 0) p.sumd[static_cast<int64_t>(kb) * rows + grow] = sumD;
+}
+
+// The carries: one thread per (row, state).  Forward: every block's start state from h0 and the
+// blocks' end states, h ← 2^(A·log2e·ΣΔ)·h + e.  Backward: every block's end gradient from dh_last,
+// g ← 2^(A·log2e·ΣΔ)·g + f, block by block from the last.
+__global__ void __launch_bounds__(256) selscan_bwd_carry_kernel(const BwdParams p) {
+  const int64_t rows = p.batch * p.dim;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = tid / kNS;
+  const int n = static_cast<int>(tid % kNS);
+  if (row >= rows) return;
+  const int N = p.dstate;
+  const int nb = p.nblocks;
+  const int64_t d = row % p.dim;
+  const float a2 = n < N ? p.A[d * N + n] * kLog2e : 0.f;
+  float h = (n < N && p.h0) ? p.h0[row * N + n] : 0.f;
+  for (int k = 0; k < nb; k++) {
+    p.hstart[(static_cast<int64_t>(k) * rows + row) * kNS + n] = h;
+    const int64_t s = static_cast<int64_t>(k) * rows + row;
+    h = fmaf(ex2_approx(a2 * p.sumd[s]), h, p.summ[s * (2 * kNS) + n]);
+  }
+  float g = (n < N && p.dh_last) ? p.dh_last[row * N + n] : 0.f;
+  for (int k = nb - 1; k >= 0; k--) {
+    p.gend[(static_cast<int64_t>(k) * rows + row) * kNS + n] = g;
+    const int64_t s = static_cast<int64_t>(k) * rows + row;
+    g = fmaf(ex2_approx(a2 * p.sumd[s]), g, p.summ[s * (2 * kNS) + kNS + n]);
+  }
+}
+
+// Time blocks: enough that the CTAs of all blocks fill the resident slots once (3 CTAs per SM), with
+// blocks of at least 256 steps; one block when the rows alone fill the GPU.  SELSCAN_BWD_TBLOCKS forces
+// a count.
+struct BwdPlan {
+  int nblocks;
+  int64_t tblock;
+};
+BwdPlan plan_bwd(int64_t batch, int64_t dim, int64_t L) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms = v > 0 ? v : 148;
+  }
+  const int64_t ctas = ((dim + kRows - 1) / kRows) * batch, slots = static_cast<int64_t>(sms) * 3;
+  int64_t nb = 1;
+  const char* env = getenv("SELSCAN_BWD_TBLOCKS");
+  if (env) {
+    nb = atoi(env);
+  } else if (2 * ctas < slots) {
+    nb = slots / (ctas > 0 ? ctas : 1);
+    const int64_t by_len = L / 256;
+    if (nb > by_len) nb = by_len;
+  }
+  if (nb < 1) nb = 1;
+  int64_t tb = (L + nb - 1) / nb;
+  tb = (tb + kBT - 1) / kBT * kBT;
+  if (tb < kBT) tb = kBT;
+  BwdPlan pl;
+  pl.tblock = tb;
+  pl.nblocks = static_cast<int>((L + tb - 1) / tb);
+  if (pl.nblocks < 1) pl.nblocks = 1;
+  return pl;
+}
+
+size_t align_floats(size_t n) { return (n + 3) / 4 * 4; }
+
 template <typename Tin, typename Tg>
 cudaError_t launch_typed(const BwdParams& p, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((p.dim + kRows - 1) / kRows), static_cast<unsigned>(p.batch));
+  const dim3 grid(static_cast<unsigned>((p.dim + kRows - 1) / kRows), static_cast<unsigned>(p.batch),
+                  static_cast<unsigned>(p.nblocks));
   const int smem = static_cast<int>(sizeof(BwdSmem));
   cudaError_t e =
       cudaFuncSetAttribute(selscan_bwd_kernel<Tin, Tg>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (p.nblocks > 1) {
+    e = cudaFuncSetAttribute(selscan_bwd_summary_kernel<Tin, Tg>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    selscan_bwd_summary_kernel<Tin, Tg><<<grid, kThreads, smem, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t threads = p.batch * p.dim * kNS;
+    selscan_bwd_carry_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(2);
+  }
   selscan_bwd_kernel<Tin, Tg><<<grid, kThreads, smem, s>>>(p);
   count_launches(1);
   return cudaGetLastError();
@@ -466,8 +672,15 @@ cudaError_t launch_typed(const BwdParams& p, cudaStream_t s) {
 
 }  // namespace
 
-size_t bwd_workspace_bytes(int64_t rows, int64_t seqlen) {
-  return sizeof(float) * static_cast<size_t>(rows) * static_cast<size_t>((seqlen + kBT - 1) / kBT) * kNS;
+size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen) {
+  const size_t rows = static_cast<size_t>(batch) * static_cast<size_t>(dim);
+  size_t floats = rows * static_cast<size_t>((seqlen + kBT - 1) / kBT) * kNS;  // checkpoints
+  const BwdPlan pl = plan_bwd(batch, dim, seqlen);
+  if (pl.nblocks > 1) {
+    const size_t nb = static_cast<size_t>(pl.nblocks);
+    floats += nb * rows * 2 * kNS + align_floats(nb * rows) + 2 * nb * rows * kNS;
+  }
+  return sizeof(float) * floats;
 }
 
 cudaError_t launch_bwd(const BwdParams& p_in, selscan_dtype_t in_dtype, selscan_dtype_t dout_dtype, void* workspace,
@@ -475,11 +688,21 @@ cudaError_t launch_bwd(const BwdParams& p_in, selscan_dtype_t in_dtype, selscan_
   BwdParams p = p_in;
   void* own = nullptr;
   if (!workspace) {
-    const cudaError_t e = cudaMallocAsync(&own, bwd_workspace_bytes(p.batch * p.dim, p.seqlen), s);
+    const cudaError_t e = cudaMallocAsync(&own, bwd_workspace_bytes(p.batch, p.dim, p.seqlen), s);
     if (e != cudaSuccess) return e;
     workspace = own;
   }
+  const BwdPlan pl = plan_bwd(p.batch, p.dim, p.seqlen);
+  const size_t rows = static_cast<size_t>(p.batch * p.dim), nb = static_cast<size_t>(pl.nblocks);
+  p.nblocks = pl.nblocks;
+  p.tblock = pl.tblock;
   p.ckpt = static_cast<float*>(workspace);
+  if (pl.nblocks > 1) {
+    p.summ = p.ckpt + rows * static_cast<size_t>((p.seqlen + kBT - 1) / kBT) * kNS;
+    p.sumd = p.summ + nb * rows * 2 * kNS;
+    p.hstart = p.sumd + align_floats(nb * rows);
+    p.gend = p.hstart + nb * rows * kNS;
+  }
   cudaError_t e;
   if (in_dtype == SELSCAN_F32)
     e = dout_dtype == SELSCAN_F32 ? launch_typed<float, float>(p, s) : launch_typed<float, __nv_bfloat16>(p, s);

@@ -96,14 +96,24 @@ struct BwdParams {
   float* ddelta_bias;  // nullable
   float* dh0;          // nullable
   float* ckpt;         // workspace: the state at the start of every chunk, [rows][chunks][16]
+  // Time blocks (nblocks > 1): blocks of tblock steps (a multiple of the chunk), their summaries
+  // (zero-start end state and zero-end start gradient, [nblocks][rows][32]; ΣΔ, [nblocks][rows]) and
+  // the carried start state and end gradient of every block ([nblocks][rows][16] each).
+  int nblocks;
+  int64_t tblock;
+  float* summ;
+  float* sumd;
+  float* hstart;
+  float* gend;
   int delta_softplus;
   int vec_in;    // u, delta, z may be read four steps at a time (8- or 16-byte loads)
   int vec_dout;  // dout may be read four steps at a time
   int vec_grad;  // du, ddelta, dz may be written four steps at a time (8- or 16-byte stores)
   int vec_dbc;   // dB, dC may take 16-byte atomic adds
 };
-// Bytes of the backward's workspace (chunk checkpoints) for `rows` = batch * dim rows.
-size_t bwd_workspace_bytes(int64_t rows, int64_t seqlen);
+// Bytes of the backward's workspace (chunk checkpoints, and the time blocks' summaries and carries when
+// the problem has too few rows to fill the current device).
+size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen);
 // The backward: zeroing of the accumulated gradients is the caller's; `workspace` (nullable: taken from
 // the stream's memory pool) holds at least bwd_workspace_bytes.
 cudaError_t launch_bwd(const BwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t dout_dtype, void* workspace,

@@ -58,6 +58,30 @@ def test_bwd_matches_oracle(i):
     check_grads(got, ref, dt, what=f"case {CASES[i][:6]}")
 
 
+# (batch, dim, seqlen, dstate, in_dtype, dout_dtype, options) run in forced time blocks
+TBLOCK_CASES = [
+    (1, 40, 700, 16, "f32", "f32", {}),
+    (2, 33, 517, 12, "bf16", "bf16", {}),
+    (1, 64, 1000, 16, "f32", "f32", {"has_z": False, "has_h0": False}),
+    (1, 24, 333, 4, "f32", "f32", {"softplus": False, "has_dh_last": False}),
+]
+
+
+@pytest.mark.parametrize("nblocks", ["2", "3", "7"])
+@pytest.mark.parametrize("i", range(len(TBLOCK_CASES)))
+def test_bwd_time_blocks(i, nblocks, monkeypatch):
+    """Time blocks (summary, carry and block-wise passes) give every gradient of the one-block run, up to
+    rounding: the carried start states and end gradients are exact in real arithmetic."""
+    monkeypatch.setenv("SELSCAN_BWD_TBLOCKS", nblocks)
+    B, Dm, L, N, dt, gdt, opt = TBLOCK_CASES[i]
+    inp, cot = _case(700 + i, B, Dm, L, N, dt, gdt, opt)
+    sp = opt.get("softplus", True)
+    got = gpu_bwd(inp, cot, delta_softplus=sp)
+    go, gh = oracle_cotangent(cot)
+    ref = oracle.selscan_bwd(inp, go, gh, delta_softplus=sp)
+    check_grads(got, ref, dt, what=f"time blocks {nblocks} case {TBLOCK_CASES[i][:6]}")
+
+
 def test_bwd_absent_optional_inputs_give_gradient_at_zero():
     """dD and dΔ_bias are returned even without D and Δ_bias: they equal the gradients at D = 0 and
     Δ_bias = 0, which the oracle computes when given explicit zeros."""
@@ -129,15 +153,20 @@ def test_bwd_requires_dz_with_z():
     assert ss.selscan_last_launch_count() == 0
 
 
-def test_bwd_launches_one_kernel():
+def test_bwd_launch_count(monkeypatch):
+    """One kernel for one time block; three (summary, carry, block-wise backward) for several."""
     import selective_state_space_152_b300 as ss
 
     inp, cot = _case(44, 1, 32, 64, 16, "f32", "f32", {})
+    monkeypatch.setenv("SELSCAN_BWD_TBLOCKS", "1")
     gpu_bwd(inp, cot)
     assert ss.selscan_last_launch_count() == 1
+    monkeypatch.setenv("SELSCAN_BWD_TBLOCKS", "2")
+    gpu_bwd(inp, cot)
+    assert ss.selscan_last_launch_count() == 3
 
 
-@pytest.mark.parametrize("name", ["mamba130m_layer", "width_2p8b"])
+@pytest.mark.parametrize("name", ["mamba130m_layer", "width_2p8b", "long_seq_65k"])
 def test_bwd_workload_full(name):
     """Every gradient of a full-size workload against the oracle on all host cores."""
     w = si.WORKLOADS[name]
