@@ -28,6 +28,7 @@
 // per (tensor, state, 4 steps) goes to global memory.  dA, dD and dΔ_bias are summed in registers over
 // the sequence and added with one atomic per row and value.
 #include <cstdlib>
+#include <type_traits>
 
 #include "selscan_internal.cuh"
 
@@ -254,17 +255,24 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
         xq = load_quad(x_row + static_cast<int64_t>(c + 1) * kBT, quad_len(nlen, q), p.vec_in);
       }
       __syncthreads();
+      // Whole chunks (all but possibly the last) run without per-step bounds checks.
+      auto scan = [&](auto whole) {
 #pragma unroll
-      for (int i = 0; i < kBT; i++) {
-        if (i >= len) break;
-        const float dl = from_prep(dlq, i, r), du = from_prep(duq, i, r);
-        const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
-        const float2 d2 = f2(dl, dl), du2 = f2(du, du);
-        const float2 e0 = mul2s(d2, A2[0]), e1 = mul2s(d2, A2[1]);
-        const float2 a0 = f2(ex2_approx(e0.x), ex2_approx(e0.y)), a1 = f2(ex2_approx(e1.x), ex2_approx(e1.y));
-        h[0] = fma2s(a0, h[0], mul2s(du2, f2(Bv.x, Bv.y)));
-        h[1] = fma2s(a1, h[1], mul2s(du2, f2(Bv.z, Bv.w)));
-      }
+        for (int i = 0; i < kBT; i++) {
+          if (!decltype(whole)::value && i >= len) break;
+          const float dl = from_prep(dlq, i, r), du = from_prep(duq, i, r);
+          const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
+          const float2 d2 = f2(dl, dl), du2 = f2(du, du);
+          const float2 e0 = mul2s(d2, A2[0]), e1 = mul2s(d2, A2[1]);
+          const float2 a0 = f2(ex2_approx(e0.x), ex2_approx(e0.y)), a1 = f2(ex2_approx(e1.x), ex2_approx(e1.y));
+          h[0] = fma2s(a0, h[0], mul2s(du2, f2(Bv.x, Bv.y)));
+          h[1] = fma2s(a1, h[1], mul2s(du2, f2(Bv.z, Bv.w)));
+        }
+      };
+      if (len == kBT)
+        scan(std::true_type{});
+      else
+        scan(std::false_type{});
     }
   }
 
@@ -340,91 +348,99 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
       gq = load_quad(go_row + o, n1, p.vec_dout);
     }
     __syncthreads();
-    // Rerun the chunk from its checkpoint: h_{t-1} of every step to shared memory, y for dz.
-    float dlv[kBT], duv[kBT], dyv[kBT], dzs[4] = {0.f, 0.f, 0.f, 0.f};
+    // Whole chunks (all but possibly the first) run without per-step bounds checks.
+    auto rerun_and_sweep = [&](auto whole) {
+      constexpr bool W = decltype(whole)::value;
+      // Rerun the chunk from its checkpoint: h_{t-1} of every step to shared memory, y for dz.
+      float dlv[kBT], duv[kBT], dyv[kBT], dzs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < kBT; i++) {
-      if (i >= len) {
-        dlv[i] = duv[i] = dyv[i] = 0.f;
-        continue;
+      for (int i = 0; i < kBT; i++) {
+        if (!W && i >= len) {
+          dlv[i] = duv[i] = dyv[i] = 0.f;
+          continue;
+        }
+        const float dl = from_prep(dlq, i, r), du = from_prep(duq, i, r);
+        dlv[i] = dl;
+        duv[i] = du;
+        dyv[i] = from_prep(dyq, i, r);
+        *reinterpret_cast<float4*>(sm.h[warp][i][lane]) = make_float4(hc[0].x, hc[0].y, hc[1].x, hc[1].y);
+        const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
+        const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
+        const float2 d2 = f2(dl, dl), du2 = f2(du, du);
+        const float2 e0 = mul2s(d2, A2[0]), e1 = mul2s(d2, A2[1]);
+        const float2 a0 = f2(ex2_approx(e0.x), ex2_approx(e0.y)), a1 = f2(ex2_approx(e1.x), ex2_approx(e1.y));
+        hc[0] = fma2s(a0, hc[0], mul2s(du2, f2(Bv.x, Bv.y)));
+        hc[1] = fma2s(a1, hc[1], mul2s(du2, f2(Bv.z, Bv.w)));
+        if (has_z) {
+          const float2 yp2 = fma2s(f2(Cv.z, Cv.w), hc[1], mul2s(f2(Cv.x, Cv.y), hc[0]));
+          const float y = row_sum(yp2.x + yp2.y);
+          if ((i >> 2) == q) dzs[i & 3] = fmaf(Dd, uqv[i & 3], y) * fzq[i & 3];
+        }
       }
-      const float dl = from_prep(dlq, i, r), du = from_prep(duq, i, r);
-      dlv[i] = dl;
-      duv[i] = du;
-      dyv[i] = from_prep(dyq, i, r);
-      *reinterpret_cast<float4*>(sm.h[warp][i][lane]) = make_float4(hc[0].x, hc[0].y, hc[1].x, hc[1].y);
-      const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
-      const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
-      const float2 d2 = f2(dl, dl), du2 = f2(du, du);
-      const float2 e0 = mul2s(d2, A2[0]), e1 = mul2s(d2, A2[1]);
-      const float2 a0 = f2(ex2_approx(e0.x), ex2_approx(e0.y)), a1 = f2(ex2_approx(e1.x), ex2_approx(e1.y));
-      hc[0] = fma2s(a0, hc[0], mul2s(du2, f2(Bv.x, Bv.y)));
-      hc[1] = fma2s(a1, hc[1], mul2s(du2, f2(Bv.z, Bv.w)));
-      if (has_z) {
-        const float2 yp2 = fma2s(f2(Cv.z, Cv.w), hc[1], mul2s(f2(Cv.x, Cv.y), hc[0]));
-        const float y = row_sum(yp2.x + yp2.y);
-        if ((i >> 2) == q) dzs[i & 3] = fmaf(Dd, uqv[i & 3], y) * fzq[i & 3];
-      }
-    }
-    if (has_z && row_ok && nq > 0) store4(static_cast<Tin*>(p.dz) + grow * L + t0 + 4 * q, nq, p.vec_grad, dzs);
-    __syncwarp();
-    // The reverse sweep of the chunk; hn holds h_t (the state after the step being undone).
-    float2 hn[2] = {hc[0], hc[1]};
-    float dus[4] = {0.f, 0.f, 0.f, 0.f}, dxs[4] = {0.f, 0.f, 0.f, 0.f};
+      if (has_z && row_ok && nq > 0) store4(static_cast<Tin*>(p.dz) + grow * L + t0 + 4 * q, nq, p.vec_grad, dzs);
+      __syncwarp();
+      // The reverse sweep of the chunk; hn holds h_t (the state after the step being undone).
+      float2 hn[2] = {hc[0], hc[1]};
+      float dus[4] = {0.f, 0.f, 0.f, 0.f}, dxs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = kBT - 1; i >= 0; i--) {
-      if (i >= len) continue;
-      const float4 hp4 = *reinterpret_cast<const float4*>(sm.h[warp][i][lane]);
-      const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
-      const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
-      const float2 hp[2] = {f2(hp4.x, hp4.y), f2(hp4.z, hp4.w)};
-      const float2 B2[2] = {f2(Bv.x, Bv.y), f2(Bv.z, Bv.w)}, C2[2] = {f2(Cv.x, Cv.y), f2(Cv.z, Cv.w)};
-      const float dl = dlv[i], dy = dyv[i];
-      const float2 d2 = f2(dl, dl), dy2 = f2(dy, dy), du2 = f2(duv[i], duv[i]);
-      float2 sGB = f2(0.f, 0.f), sAGw = f2(0.f, 0.f), vB[2], vC[2];
+      for (int i = kBT - 1; i >= 0; i--) {
+        if (!W && i >= len) continue;
+        const float4 hp4 = *reinterpret_cast<const float4*>(sm.h[warp][i][lane]);
+        const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
+        const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
+        const float2 hp[2] = {f2(hp4.x, hp4.y), f2(hp4.z, hp4.w)};
+        const float2 B2[2] = {f2(Bv.x, Bv.y), f2(Bv.z, Bv.w)}, C2[2] = {f2(Cv.x, Cv.y), f2(Cv.z, Cv.w)};
+        const float dl = dlv[i], dy = dyv[i];
+        const float2 d2 = f2(dl, dl), dy2 = f2(dy, dy), du2 = f2(duv[i], duv[i]);
+        float2 sGB = f2(0.f, 0.f), sAGw = f2(0.f, 0.f), vB[2], vC[2];
 #pragma unroll
-      for (int k = 0; k < 2; k++) {
-        const float2 e = mul2s(d2, A2[k]);
-        const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
-        const float2 G = fma2s(dy2, C2[k], g[k]);
-        const float2 t = mul2s(G, mul2s(ab, hp[k]));  // G Ā h_{t-1}
-        vB[k] = mul2s(G, du2);                        // this row's dB
-        vC[k] = mul2s(dy2, hn[k]);                    // this row's dC
-        sGB = fma2s(G, B2[k], sGB);
-        sAGw = fma2s(Ar[k], t, sAGw);
-        dA[k] = fma2s(t, d2, dA[k]);
-        g[k] = mul2s(G, ab);
-        hn[k] = hp[k];
-      }
-      // dB, dC: the sum over the warp's 8 rows by recursive halving; lane 8q + r ends with value r of
-      // {dB of states 4q..4q+3, dC of states 4q..4q+3}.
-      const float v[8] = {vB[0].x, vB[0].y, vB[1].x, vB[1].y, vC[0].x, vC[0].y, vC[1].x, vC[1].y};
-      float w4[4], w2[2];
+        for (int k = 0; k < 2; k++) {
+          const float2 e = mul2s(d2, A2[k]);
+          const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
+          const float2 G = fma2s(dy2, C2[k], g[k]);
+          const float2 t = mul2s(G, mul2s(ab, hp[k]));  // G Ā h_{t-1}
+          vB[k] = mul2s(G, du2);                        // this row's dB
+          vC[k] = mul2s(dy2, hn[k]);                    // this row's dC
+          sGB = fma2s(G, B2[k], sGB);
+          sAGw = fma2s(Ar[k], t, sAGw);
+          dA[k] = fma2s(t, d2, dA[k]);
+          g[k] = mul2s(G, ab);
+          hn[k] = hp[k];
+        }
+        // dB, dC: the sum over the warp's 8 rows by recursive halving; lane 8q + r ends with value r of
+        // {dB of states 4q..4q+3, dC of states 4q..4q+3}.
+        const float v[8] = {vB[0].x, vB[0].y, vB[1].x, vB[1].y, vC[0].x, vC[0].y, vC[1].x, vC[1].y};
+        float w4[4], w2[2];
 #pragma unroll
-      for (int j = 0; j < 4; j++) {
-        const float send = b2 ? v[j] : v[4 + j];
-        w4[j] = (b2 ? v[4 + j] : v[j]) + __shfl_xor_sync(kFull, send, 4);
-      }
+        for (int j = 0; j < 4; j++) {
+          const float send = b2 ? v[j] : v[4 + j];
+          w4[j] = (b2 ? v[4 + j] : v[j]) + __shfl_xor_sync(kFull, send, 4);
+        }
 #pragma unroll
-      for (int j = 0; j < 2; j++) {
-        const float send = b1 ? w4[j] : w4[2 + j];
-        w2[j] = (b1 ? w4[2 + j] : w4[j]) + __shfl_xor_sync(kFull, send, 2);
+        for (int j = 0; j < 2; j++) {
+          const float send = b1 ? w4[j] : w4[2 + j];
+          w2[j] = (b1 ? w4[2 + j] : w4[j]) + __shfl_xor_sync(kFull, send, 2);
+        }
+        sm.red[warp][i][lane] = (b0 ? w2[1] : w2[0]) + __shfl_xor_sync(kFull, b0 ? w2[0] : w2[1], 1);
+        const float S = row_sum(sGB.x + sGB.y), T = row_sum(sAGw.x + sAGw.y);
+        if ((i >> 2) == q) {  // the lane that prepared this step stores its gradients
+          const int m = i & 3;
+          const float dx = fmaf(uqv[m], S, T) * sgq[m];
+          dus[m] = fmaf(dy, Dd, dl * S);
+          dxs[m] = dx;
+          dD = fmaf(dy, uqv[m], dD);
+          dbias += dx;
+        }
       }
-      sm.red[warp][i][lane] = (b0 ? w2[1] : w2[0]) + __shfl_xor_sync(kFull, b0 ? w2[0] : w2[1], 1);
-      const float S = row_sum(sGB.x + sGB.y), T = row_sum(sAGw.x + sAGw.y);
-      if ((i >> 2) == q) {  // the lane that prepared this step stores its gradients
-        const int m = i & 3;
-        const float dx = fmaf(uqv[m], S, T) * sgq[m];
-        dus[m] = fmaf(dy, Dd, dl * S);
-        dxs[m] = dx;
-        dD = fmaf(dy, uqv[m], dD);
-        dbias += dx;
+      if (row_ok && nq > 0) {
+        store4(static_cast<Tin*>(p.du) + grow * L + t0 + 4 * q, nq, p.vec_grad, dus);
+        store4(static_cast<Tin*>(p.ddelta) + grow * L + t0 + 4 * q, nq, p.vec_grad, dxs);
       }
-    }
-    if (row_ok && nq > 0) {
-      store4(static_cast<Tin*>(p.du) + grow * L + t0 + 4 * q, nq, p.vec_grad, dus);
-      store4(static_cast<Tin*>(p.ddelta) + grow * L + t0 + 4 * q, nq, p.vec_grad, dxs);
-    }
+    };
+    if (len == kBT)
+      rerun_and_sweep(std::true_type{});
+    else
+      rerun_and_sweep(std::false_type{});
     __syncthreads();
     // dB, dC of the chunk: the CTA's warps added up, then one atomic add per (tensor, state, 4 steps).
     {
