@@ -178,7 +178,8 @@ def max_over_ranks(seconds, dist, device):
 
 # The sources each kernel is built from (its own file and the shared device helpers).
 KERNEL_SOURCES = {"selscan_fwd": ("selscan_rows.cu", "selscan_fwd.cu", "selscan_fwd_seq.cu", "selscan_internal.cuh"),
-                  "selscan_step": ("selscan_step.cu", "selscan_internal.cuh")}
+                  "selscan_step": ("selscan_step.cu", "selscan_internal.cuh"),
+                  "selscan_bwd": ("selscan_bwd.cu", "selscan_internal.cuh")}
 
 
 def kernel_source_hash(kernel=None):
@@ -646,7 +647,8 @@ def run_backward(args, torch, ss, device, stream, flush, sms, hbm_gbs, sm_mhz, r
         wk = bwd_work(Bsz, Dm, L, N, in_bytes=2 if w.in_dtype == "bf16" else 4, dout_bytes=2)
         res[name] = {"batch": Bsz, "dim": Dm, "seqlen": L, "dstate": N, "dout_dtype": "bf16",
                      "us_per_call": secs * 1e6, "elems_per_s": wk["elements"] / secs,
-                     "roofline": roofline_entry(wk, secs, sms, hbm_gbs, sm_mhz, rates=rates),
+                     "roofline": roofline_entry(wk, secs, sms, hbm_gbs, sm_mhz, rates=rates,
+                                                traffic=recorded_traffic("selscan_bwd", name)),
                      "launches_per_call": launches, "gpu_launches": launches * reps}
         del t, g, ws, go, gh
     return res
