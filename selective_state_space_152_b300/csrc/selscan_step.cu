@@ -8,7 +8,6 @@
 // D >= 64, four threads per row with B and C staged per CTA (selscan_step_quad_kernel); otherwise
 // Q = NS/4 consecutive threads per row, each owning four states (one 16-byte vector), the Q partial
 // sums of y meeting with shuffles.  A one-thread-per-row kernel stays selectable for comparison.
-#include <climits>
 #include <cstdlib>
 
 #include "selscan_internal.cuh"
@@ -159,18 +158,12 @@ __device__ __forceinline__ float4 load_quad(const Tin* p) {
 
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(256) selscan_step_quad_kernel(const StepParams p) {
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
-  const int64_t rows = p.batch * p.dim;
-  const int64_t row = gid >> 2;
+  // Grid (channel blocks of 64, batch entries): the row's batch entry and channel come from the grid.
   const int q = threadIdx.x & 3;
-  if (row >= rows) return;  // whole rows leave together (4 divides the warp)
-  int64_t b;
-  if (rows <= INT32_MAX) {  // 32-bit division where the row index fits
-    b = static_cast<uint32_t>(row) / static_cast<uint32_t>(p.dim);
-  } else {
-    b = row / p.dim;
-  }
-  const int64_t d = row - b * p.dim;
+  const int64_t b = blockIdx.y;
+  const int64_t d = static_cast<int64_t>(blockIdx.x) * 64 + (threadIdx.x >> 2);
+  if (d >= p.dim) return;  // whole rows leave together (4 divides the warp)
+  const int64_t row = b * p.dim + d;
   float4 h = __ldcs(reinterpret_cast<const float4*>(p.state + row * 16) + q);
   const float4 a = __ldg(reinterpret_cast<const float4*>(p.A + d * 16) + q);
   const float4 bv = load_quad(static_cast<const Tin*>(p.B) + b * 16 + 4 * q);
@@ -179,6 +172,8 @@ __global__ void __launch_bounds__(256) selscan_step_quad_kernel(const StepParams
   const float x = to_f32(static_cast<const Tin*>(p.delta)[row]) + (p.delta_bias ? p.delta_bias[d] : 0.f);
   const float zz = p.z ? to_f32(static_cast<const Tin*>(p.z)[row]) : 0.f;
   const float Dd = p.D ? p.D[d] : 0.f;
+  // Each of the row's four threads forms Δ itself: a divergent branch would cost the warp the same
+  // issue slots and add a shuffle's latency.
   const float dt = p.delta_softplus ? softplus_fast(x) : x;
   const float dtl = dt * kLog2e, du = dt * uu;
   h.x = fmaf(ex2_approx(dtl * a.x), h.x, du * bv.x);
@@ -201,9 +196,9 @@ cudaError_t launch_ns(const StepParams& p, cudaStream_t s) {
   // SELSCAN_STEP: "quad", "row" or "generic" (default: the first that applies).
   const char* force = getenv("SELSCAN_STEP");
   const char f = force ? force[0] : 'q';
-  if (f == 'q' && NS == 16 && p.dstate == 16 && p.vec_state && p.vec_bc) {
-    const int64_t rows = p.batch * p.dim;
-    selscan_step_quad_kernel<Tin, Tout><<<static_cast<unsigned>((rows + 63) / 64), 256, 0, s>>>(p);
+  if (f == 'q' && NS == 16 && p.dstate == 16 && p.vec_state && p.vec_bc && p.batch <= 65535) {
+    const dim3 grid(static_cast<unsigned>((p.dim + 63) / 64), static_cast<unsigned>(p.batch));
+    selscan_step_quad_kernel<Tin, Tout><<<grid, 256, 0, s>>>(p);
     count_launches(1);
     return cudaGetLastError();
   }
