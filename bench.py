@@ -176,8 +176,9 @@ def max_over_ranks(seconds, dist, device):
     return float(tt.item())
 
 
-# The sources each kernel is built from (its own file and the shared device helpers).
-KERNEL_SOURCES = {"selscan_fwd": ("selscan_rows.cu", "selscan_fwd.cu", "selscan_fwd_seq.cu", "selscan_internal.cuh"),
+# The sources each measured kernel is built from (its own file and the shared device helpers): the forward
+# workloads run the row-sequential kernel.
+KERNEL_SOURCES = {"selscan_fwd": ("selscan_rows.cu", "selscan_internal.cuh"),
                   "selscan_step": ("selscan_step.cu", "selscan_internal.cuh"),
                   "selscan_bwd": ("selscan_bwd.cu", "selscan_internal.cuh")}
 

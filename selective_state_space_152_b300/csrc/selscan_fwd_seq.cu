@@ -630,9 +630,13 @@ int64_t choose_tblock(const FwdParams& p, int64_t row_blocks, int slots) {
   return tb;
 }
 
+// One forward call of the sequential kernel: one pass, or time blocks whose scratch comes from the
+// stream's memory pool or (ScratchSource::Fixed, selscan_fwd_noalloc) the library's fixed array; with the
+// fixed array *too_big is set and nothing enqueued when the blocks need more than it holds.
 template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS, bool REV = false,
           bool ZOH = false, bool CONV = false>
-cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
+cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s, ScratchSource src = ScratchSource::Pool,
+                           bool* too_big = nullptr) {
   using C = SeqCfg<NS, Q, R, Tin>;
   FwdParams p = p_in;
   TmaMaps maps;
@@ -671,14 +675,29 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
     count_launches(1);
     return cudaGetLastError();
   }
-  // Stream-ordered scratch for the block summaries and start states, released on the same stream.  If
-  // the pool cannot supply it the call fails with the allocation error (selscan_fwd_noalloc needs none).
   const int64_t N = p.dstate;
   const size_t summ_floats = static_cast<size_t>(p.nblocks - 1) * rows * (N + 1);
   const size_t start_floats = static_cast<size_t>(p.nblocks) * rows * N;
+  const size_t bytes = (summ_floats + start_floats) * sizeof(float);
   void* ws = nullptr;
-  e = cudaMallocAsync(&ws, (summ_floats + start_floats) * sizeof(float), s);
-  if (e != cudaSuccess) return e;
+  if (src == ScratchSource::Fixed) {
+    // Every summary entry is written by the summary pass and every start entry by the carry pass before
+    // it is read, so nothing in the array needs clearing.
+    float* fixed = nullptr;
+    size_t cap_bytes = 0;
+    e = fixed_scratch(&fixed, &cap_bytes);
+    if (e != cudaSuccess) return e;
+    if (bytes > cap_bytes) {
+      if (too_big) *too_big = true;
+      return cudaSuccess;
+    }
+    ws = fixed;
+  } else {
+    // Stream-ordered scratch for the block summaries and start states, released on the same stream.  If
+    // the pool cannot supply it the call fails with the allocation error (selscan_fwd_noalloc needs none).
+    e = cudaMallocAsync(&ws, bytes, s);
+    if (e != cudaSuccess) return e;
+  }
   p.summ = static_cast<float*>(ws);
   p.start = p.summ + summ_floats;
   const dim3 sgrid(grid.x, grid.y, grid.z - 1);
@@ -696,6 +715,7 @@ cudaError_t launch_seq_cfg(const FwdParams& p_in, cudaStream_t s) {
     count_launches(1);
     e = cudaGetLastError();
   }
+  if (src == ScratchSource::Fixed) return e;
   const cudaError_t ef = cudaFreeAsync(ws, s);
   return e != cudaSuccess ? e : ef;
 }
@@ -768,86 +788,14 @@ cudaError_t launch_fwd_seq(const FwdParams& p, selscan_dtype_t in_dtype, selscan
 
 namespace {
 
-// As launch_seq_cfg, with the scratch taken from the fixed array.
-template <int NS, int Q, int R, typename Tin, typename Tout, bool FULLN, bool SOFTPLUS>
-cudaError_t launch_seq_noalloc_cfg(const FwdParams& p_in, cudaStream_t s, bool* too_big) {
-  using C = SeqCfg<NS, Q, R, Tin>;
-  FwdParams p = p_in;
-  TmaMaps maps;
-  memset(&maps, 0, sizeof maps);
-  const EncodeTiled enc = reinterpret_cast<EncodeTiled>(tensor_map_encoder());
-  const uint64_t rows = static_cast<uint64_t>(p.batch * p.dim), bc_rows = static_cast<uint64_t>(p.batch * p.dstate);
-  p.use_tma = p.vec_stage && enc && rows < (1ull << 31) && p.seqlen < (1ll << 31);
-  if (p.use_tma) {
-    const uint64_t L = static_cast<uint64_t>(p.seqlen);
-    bool ok = encode_2d<Tin>(enc, &maps.u, p.u, L, rows, C::EPR, C::ROWS, C::kSwizzle) &&
-              encode_2d<Tin>(enc, &maps.delta, p.delta, L, rows, C::EPR, C::ROWS, C::kSwizzle) &&
-              (!p.z || encode_2d<Tin>(enc, &maps.z, p.z, L, rows, C::EPR, C::ROWS, C::kSwizzle)) &&
-              encode_2d<Tin>(enc, &maps.B, p.B, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              encode_2d<Tin>(enc, &maps.C, p.C, L, bc_rows, C::T, NS, CU_TENSOR_MAP_SWIZZLE_NONE);
-    p.use_tma = ok;
-  }
-  auto scan = selscan_fwd_seq_kernel<NS, Q, R, Tin, Tout, FULLN, SOFTPLUS, false>;
-  auto summary = selscan_fwd_seq_kernel<NS, Q, R, Tin, float, FULLN, SOFTPLUS, true>;
-  cudaError_t e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(summary, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
-  if (e != cudaSuccess) return e;
-  const int64_t row_blocks = ((p.dim + C::ROWS - 1) / C::ROWS) * p.batch;
-  int per_sm = 0, sms = 0, dev = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scan, R * 32, C::kSmem) != cudaSuccess || per_sm < 1)
-    per_sm = 1;
-  p.tblock = choose_tblock(p, row_blocks, sms * per_sm);
-  p.nblocks = static_cast<int>((p.seqlen + p.tblock - 1) / p.tblock);
-  const dim3 grid(static_cast<unsigned>((p.dim + C::ROWS - 1) / C::ROWS), static_cast<unsigned>(p.batch),
-                  static_cast<unsigned>(p.nblocks));
-  if (p.nblocks == 1) {  // one pass: no scratch needed
-    scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
-    count_launches(1);
-    return cudaGetLastError();
-  }
-  const int64_t N = p.dstate;
-  const size_t summ_floats = static_cast<size_t>(p.nblocks - 1) * rows * (N + 1);
-  const size_t start_floats = static_cast<size_t>(p.nblocks) * rows * N;
-  float* ws = nullptr;
-  size_t cap_bytes = 0;
-  e = fixed_scratch(&ws, &cap_bytes);
-  if (e != cudaSuccess) return e;
-  if ((summ_floats + start_floats) * sizeof(float) > cap_bytes) {
-    *too_big = true;
-    return cudaSuccess;
-  }
-  // Every summary entry is written by the summary pass and every start entry by the carry pass
-  // before it is read, so nothing in the array needs clearing.
-  p.summ = ws;
-  p.start = ws + summ_floats;
-  const dim3 sgrid(grid.x, grid.y, grid.z - 1);
-  summary<<<sgrid, R * 32, C::kSmem, s>>>(p, maps);
-  count_launches(1);
-  e = cudaGetLastError();
-  if (e == cudaSuccess) {
-    const int64_t threads = static_cast<int64_t>(rows) * N;
-    selscan_carry_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(p);
-    count_launches(1);
-    e = cudaGetLastError();
-  }
-  if (e == cudaSuccess) {
-    scan<<<grid, R * 32, C::kSmem, s>>>(p, maps);
-    count_launches(1);
-    e = cudaGetLastError();
-  }
-  return e;
-}
-
 template <typename Tin, typename Tout, bool SOFTPLUS>
 cudaError_t dispatch_seq_noalloc_sp(const FwdParams& p, cudaStream_t s, bool* too_big) {
   constexpr int R = SELSCAN_SEQ_R;
-  if (p.dstate == 16) return launch_seq_noalloc_cfg<16, 2, R, Tin, Tout, true, SOFTPLUS>(p, s, too_big);
-  if (p.dstate <= 4) return launch_seq_noalloc_cfg<4, 1, R, Tin, Tout, false, SOFTPLUS>(p, s, too_big);
-  if (p.dstate <= 8) return launch_seq_noalloc_cfg<8, 2, R, Tin, Tout, false, SOFTPLUS>(p, s, too_big);
-  return launch_seq_noalloc_cfg<16, 2, R, Tin, Tout, false, SOFTPLUS>(p, s, too_big);
+  constexpr ScratchSource F = ScratchSource::Fixed;
+  if (p.dstate == 16) return launch_seq_cfg<16, 2, R, Tin, Tout, true, SOFTPLUS>(p, s, F, too_big);
+  if (p.dstate <= 4) return launch_seq_cfg<4, 1, R, Tin, Tout, false, SOFTPLUS>(p, s, F, too_big);
+  if (p.dstate <= 8) return launch_seq_cfg<8, 2, R, Tin, Tout, false, SOFTPLUS>(p, s, F, too_big);
+  return launch_seq_cfg<16, 2, R, Tin, Tout, false, SOFTPLUS>(p, s, F, too_big);
 }
 
 template <typename Tin, typename Tout>

@@ -387,11 +387,13 @@ def test_step_rows_spanning_batch_entries(dt):
     check_h(state.cpu().numpy().astype(np.float64), href, what="decode state")
 
 
-STEP_CASES = [(5, 100, 4, "bf16", True), (5, 192, 4, "f32", False), (1400, 256, 3, "bf16", True)]
+# (batch, dim, steps, in_dtype, has_z, out_dtype)
+STEP_CASES = [(5, 100, 4, "bf16", True, "f32"), (5, 192, 4, "f32", False, "f32"), (1400, 256, 3, "bf16", True, "f32"),
+              (3, 384, 3, "f32", False, "f32"), (2, 512, 3, "bf16", True, "bf16")]
 
 
 @pytest.mark.parametrize("kern", ["quad", "row", "generic"])
-@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: "x".join(map(str, c[:3])) + f"-{c[3]}-z{int(c[4])}")
+@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: "x".join(map(str, c[:3])) + f"-{c[3]}-z{int(c[4])}-{c[5]}")
 def test_step_kernels(case, kern, monkeypatch):
     """Each decode kernel, a few steps carrying the state, against the forward oracle (D = 100 puts a
     batch-entry boundary inside CTAs of the quad kernel, whose 64 rows then span two entries)."""
@@ -400,7 +402,7 @@ def test_step_kernels(case, kern, monkeypatch):
     import selective_state_space_152_b300 as ss
 
     monkeypatch.setenv("SELSCAN_STEP", kern)
-    Bsz, Dm, T, dt, has_z = case
+    Bsz, Dm, T, dt, has_z, odt = case
     inp = si.random_case(137 + Bsz, Bsz, Dm, T, 16, in_dtype=dt, has_z=has_z)
     ref, href = oracle.selscan_fwd(inp)
     t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
@@ -410,11 +412,13 @@ def test_step_kernels(case, kern, monkeypatch):
         z = None if t["z"] is None else t["z"][..., s].contiguous()
         outs.append(ss.selscan_step(t["u"][..., s].contiguous(), t["delta"][..., s].contiguous(), t["A"],
                                     t["B"][..., s].contiguous(), t["C"][..., s].contiguous(), state, D=t["D"],
-                                    z=z, delta_bias=t["delta_bias"]))
+                                    z=z, delta_bias=t["delta_bias"],
+                                    out_dtype=torch.bfloat16 if odt == "bf16" else torch.float32))
         assert ss.selscan_last_launch_count() == 1
     torch.cuda.synchronize()
-    got = torch.stack(outs, dim=-1).cpu().numpy().astype(np.float64)
-    check_out(got, ref, dt, what=f"decode {kern}")
+    got = torch.stack(outs, dim=-1).float().cpu().numpy().astype(np.float64)
+    # a bf16 output adds its own rounding (2^-8 relative) to the bound
+    check_out(got, ref, dt, what=f"decode {kern}", extra_rel=2.0 ** -8 if odt == "bf16" else 0.0)
     check_h(state.cpu().numpy().astype(np.float64), href, what=f"decode {kern} state")
     assert ss.selscan_device_status() == 0
 
