@@ -24,7 +24,9 @@ sequence and the 2.8B-width layer) the same way, each with its own roofline;
 ``unit_rates`` are the special-function and FMA rates measured on the GPU by the
 library's own probe (selscan_probe_rate), from which the rooflines are derived.
 ``backward`` times selscan_bwd (every gradient, bf16 dout) on the same workloads,
-each against the backward's own roofline (``bwd_work``).
+each against the backward's own roofline (``bwd_work``), and the training pair
+selscan_fwd_ckpt + selscan_bwd_ckpt (the backward rerunning from the forward's
+chunk checkpoints).
 """
 from __future__ import annotations
 
@@ -645,13 +647,42 @@ def run_backward(args, torch, ss, device, stream, flush, sms, hbm_gbs, sm_mhz, r
             e1.record(stream)
         torch.cuda.synchronize()
         secs = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
+        # The training pair: the forward keeping its chunk checkpoints, and the backward rerunning from them.
+        out = torch.empty((Bsz, Dm, L), device=device, dtype=torch.float32)
+        ck = torch.empty((Bsz, Dm, (L + 15) // 16, 16), device=device, dtype=torch.float32)
+
+        def fwd_ckpt():
+            ss.selscan_fwd_ckpt(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                                delta_bias=t["delta_bias"], h0=t["h0"], out=out, ckpt=ck, stream=stream)
+
+        def bwd_ckpt():
+            ss.selscan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], go, D=t["D"], z=t["z"],
+                           delta_bias=t["delta_bias"], h0=t["h0"], dh_last=gh, grads=g, workspace=ws, ckpt=ck,
+                           stream=stream)
+
+        pair = {}
+        for key, fn in (("fwd_ckpt_us", fwd_ckpt), ("bwd_from_ckpt_us", bwd_ckpt)):
+            for _ in range(3):
+                flush.zero_()
+                fn()
+            evp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for e0, e1 in evp:
+                flush.zero_()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            pair[key] = statistics.median(e0.elapsed_time(e1) for e0, e1 in evp) * 1e3
         wk = bwd_work(Bsz, Dm, L, N, in_bytes=2 if w.in_dtype == "bf16" else 4, dout_bytes=2)
         res[name] = {"batch": Bsz, "dim": Dm, "seqlen": L, "dstate": N, "dout_dtype": "bf16",
                      "us_per_call": secs * 1e6, "elems_per_s": wk["elements"] / secs,
                      "roofline": roofline_entry(wk, secs, sms, hbm_gbs, sm_mhz, rates=rates,
                                                 traffic=recorded_traffic("selscan_bwd", name)),
-                     "launches_per_call": launches, "gpu_launches": launches * reps}
-        del t, g, ws, go, gh
+                     "launches_per_call": launches, "gpu_launches": launches * reps,
+                     "training_pair": dict(pair, note="selscan_fwd_ckpt keeps the state before every 16-step "
+                                           "chunk; selscan_bwd_ckpt reruns chunks from it (no forward pass of "
+                                           "its own)")}
+        del t, g, ws, go, gh, out, ck
     return res
 
 

@@ -255,8 +255,39 @@ selscan_status_t selscan_bwd(const selscan_shape_t* shape, const void* u, const 
                              float* dC, float* dD, float* ddelta_bias, float* dh0, void* workspace,
                              size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace selscan_bwd needs for `shape` (0 for an invalid shape). */
+/* Bytes of workspace selscan_bwd needs for `shape` (0 for an invalid shape); enough for
+ * selscan_bwd_ckpt too, which needs less (no checkpoints of its own). */
 size_t selscan_bwd_workspace_size(const selscan_shape_t* shape);
+
+/*
+ * Training pair: a forward that keeps the state before every 16-step chunk, and a backward that reruns
+ * chunks from those checkpoints instead of recomputing them with a forward pass of its own — the
+ * checkpointed recomputation of "Mamba状态空间模型深度解析：挑战Transformer的下一代序列建模范式" §2.2,
+ * with the forward's checkpoints kept.
+ *
+ * selscan_fwd_ckpt: selscan_fwd plus
+ *   ckpt : [B, D, ceil(L/16), 16] fp32, written: ckpt[b,d,c,n] = the state h before step 16·c (h0 for
+ *          c = 0); slots of states n >= N are left unwritten.  Required when there is work.
+ * It needs the row-sequential kernel (every u, delta, z, B, C row 16-byte aligned: L a multiple of 8
+ * for bf16, of 4 for fp32, and 16-byte aligned bases); otherwise it returns SELSCAN_ERR_UNSUPPORTED and
+ * enqueues nothing.  The checkpoints cost 4 bytes of writes per element (64 bytes per row and chunk).
+ *
+ * selscan_bwd_ckpt: selscan_bwd with
+ *   ckpt : the checkpoints selscan_fwd_ckpt wrote for the same u, delta, A, B, delta_bias,
+ *          delta_softplus and h0 (read only; required when there is work).
+ * Its workspace needs no checkpoint space (selscan_bwd_workspace_size is an upper bound).  Every other
+ * argument, check and result is selscan_bwd's.
+ */
+selscan_status_t selscan_fwd_ckpt(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* D, const void* z,
+                                  const float* delta_bias, int delta_softplus, const float* h0, void* out,
+                                  float* h_last, float* ckpt, void* stream);
+selscan_status_t selscan_bwd_ckpt(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* D, const void* z,
+                                  const float* delta_bias, int delta_softplus, const float* h0, const void* dout,
+                                  const float* dh_last, const float* ckpt, void* du, void* ddelta, void* dz,
+                                  float* dA, float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* selscan_status_string(selscan_status_t status);
@@ -278,10 +309,11 @@ int selscan_abi_version(void);
 
 /*
  * The number of kernels that the last selscan_fwd, selscan_fwd_ex, selscan_fwd_conv,
- * selscan_fwd_noalloc, selscan_bwd or selscan_step call on this host thread enqueued: 1 for a
- * forward run in one pass, a backward or a decode step, 3 for a forward run in time blocks (the
- * summary pass, the carry pass and the scan), 0 when the call enqueued no kernel (an
- * argument error, no rows, or an empty sequence, whose state is passed on by a copy).
+ * selscan_fwd_noalloc, selscan_fwd_ckpt, selscan_bwd, selscan_bwd_ckpt or selscan_step call on this
+ * host thread enqueued: 1 for a forward or backward run in one pass or a decode step, 3 for a forward
+ * or backward run in time blocks (the summary pass, the carry pass and the scan), 0 when the call
+ * enqueued no kernel (an argument error, no rows, or an empty sequence, whose state is passed on by a
+ * copy).
  * The pages have no counterpart; it lets a caller (or a benchmark) account for the
  * launches of its timed region.
  */

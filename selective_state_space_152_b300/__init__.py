@@ -23,7 +23,8 @@ STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SE
           8: "SELSCAN_ERR_SCRATCH"}
 EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
             "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_probe_rate",
-            "selscan_last_launch_count", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_probe_wait_timeout")
+            "selscan_last_launch_count", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_probe_wait_timeout",
+            "selscan_fwd_ckpt", "selscan_bwd_ckpt")
 # Units of selscan_probe_rate (include/selscan_probe.h).
 PROBE_UNITS = {"ex2": 0, "lg2": 1, "rcp": 2, "tanh": 3, "ffma": 4, "ffma2": 5}
 SELSCAN_FLAG_REVERSE, SELSCAN_FLAG_ZOH = 1, 2
@@ -80,6 +81,11 @@ def load_library(path: Optional[str] = None):
     lib.selscan_bwd.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                 vp, ctypes.c_size_t, vp]
     lib.selscan_bwd.restype = i32
+    lib.selscan_fwd_ckpt.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+    lib.selscan_fwd_ckpt.restype = i32
+    lib.selscan_bwd_ckpt.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.selscan_bwd_ckpt.restype = i32
     lib.selscan_bwd_workspace_size.argtypes = [shp]
     lib.selscan_bwd_workspace_size.restype = ctypes.c_size_t
     lib.selscan_probe_wait_timeout.argtypes = [ctypes.c_int64, ctypes.POINTER(ctypes.c_int)]
@@ -214,6 +220,37 @@ def selscan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softpl
     return out, h_last
 
 
+def selscan_fwd_ckpt(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
+                     out=None, h_last=None, ckpt=None, stream=None, out_dtype=None, return_h_last: bool = False):
+    """``selscan_fwd`` that also keeps the state before every 16-step chunk for ``selscan_bwd(ckpt=...)``.
+
+    Returns ``(out, h_last, ckpt)``, ``ckpt`` [B, D, ceil(L/16), 16] float32 (allocated if not given).
+    """
+    torch = _torch()
+    lib = load_library()
+    if u.dim() != 3 or B.dim() != 3:
+        raise ValueError("u must be [B, D, L] and B must be [B, N, L]")
+    Bsz, Dm, L = u.shape
+    N = B.shape[1]
+    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias), ("h0", h0), ("h_last", h_last), ("ckpt", ckpt)):
+        _need_f32(name, t)
+    for name, t in (("delta", delta), ("z", z), ("B", B), ("C", C)):
+        if t is not None and t.dtype != u.dtype:
+            raise TypeError(f"{name} must have u's dtype {u.dtype}")
+    if out is None:
+        out = torch.empty((Bsz, Dm, L), device=u.device, dtype=out_dtype or torch.float32)
+    if h_last is None and return_h_last:
+        h_last = torch.empty((Bsz, Dm, N), device=u.device, dtype=torch.float32)
+    if ckpt is None:
+        ckpt = torch.empty((Bsz, Dm, (L + 15) // 16, 16), device=u.device, dtype=torch.float32)
+    shape = SelscanShape(Bsz, Dm, L, N, _dtype_code(u.dtype), _dtype_code(out.dtype))
+    st = lib.selscan_fwd_ckpt(ctypes.byref(shape), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                              _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(out), _ptr(h_last),
+                              _ptr(ckpt), _stream_handle(stream))
+    _check(st)
+    return out, h_last, ckpt
+
+
 def selscan_fwd_ex(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
                    out=None, h_last=None, stream=None, out_dtype=None, return_h_last: bool = False,
                    reverse: bool = False, zoh: bool = False):
@@ -338,14 +375,15 @@ def selscan_bwd_workspace_size(Bsz: int, Dm: int, L: int, N: int) -> int:
 
 
 def selscan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, delta_softplus: bool = True, h0=None,
-                dh_last=None, grads=None, workspace=None, stream=None, want_dh0: bool = True):
+                dh_last=None, grads=None, workspace=None, stream=None, want_dh0: bool = True, ckpt=None):
     """Gradients of ``selscan_fwd`` for ``dout`` = ∂loss/∂out (and ``dh_last`` = ∂loss/∂h_last, or None).
 
     Returns a dict with "u", "delta" and "z" ([B, D, L], u's dtype; "z" None without z), "A" [D, N],
     "B", "C" ([B, N, L], float32), "D", "delta_bias" ([D], float32) and "h0" ([B, D, N], float32; None
     unless ``want_dh0``).  ``grads`` may hold preallocated outputs under the same keys.  ``workspace`` is
     a CUDA tensor of at least ``selscan_bwd_workspace_size`` bytes (or None: the library takes it from
-    the stream's memory pool).
+    the stream's memory pool).  ``ckpt`` (from ``selscan_fwd_ckpt`` on the same inputs) makes it rerun
+    chunks from the forward's checkpoints (``selscan_bwd_ckpt``) instead of recomputing them.
     """
     torch = _torch()
     lib = load_library()
@@ -384,16 +422,20 @@ def selscan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, delta_
         _need_f32("grad of " + key, g.get(key))
     shape = SelscanShape(Bsz, Dm, L, N, _dtype_code(u.dtype), _dtype_code(dout.dtype))
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.selscan_bwd(ctypes.byref(shape), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                         _ptr(delta_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(dh_last),
-                         _ptr(g["u"]), _ptr(g["delta"]), _ptr(g["z"]), _ptr(g["A"]), _ptr(g["B"]), _ptr(g["C"]),
-                         _ptr(g["D"]), _ptr(g["delta_bias"]), _ptr(g["h0"]), _ptr(workspace), ws_bytes,
-                         _stream_handle(stream))
+    head = (ctypes.byref(shape), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(dh_last))
+    tail = (_ptr(g["u"]), _ptr(g["delta"]), _ptr(g["z"]), _ptr(g["A"]), _ptr(g["B"]), _ptr(g["C"]), _ptr(g["D"]),
+            _ptr(g["delta_bias"]), _ptr(g["h0"]), _ptr(workspace), ws_bytes, _stream_handle(stream))
+    if ckpt is None:
+        st = lib.selscan_bwd(*head, *tail)
+    else:
+        _need_f32("ckpt", ckpt)
+        st = lib.selscan_bwd_ckpt(*head, _ptr(ckpt), *tail)
     _check(st)
     return g
 
 
-__all__ = ["selscan_fwd", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_probe_wait_timeout", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step",
+__all__ = ["selscan_fwd", "selscan_fwd_ckpt", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_probe_wait_timeout", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step",
            "selscan_status_string", "selscan_abi_version", "selscan_last_cuda_error", "selscan_device_status",
            "selscan_probe_rate", "selscan_last_launch_count", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED",
            "PROBE_UNITS"]

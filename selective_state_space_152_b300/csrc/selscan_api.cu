@@ -150,7 +150,7 @@ selscan_status_t prepare_fwd(const selscan_shape_t* shape, const void* u, const 
                              const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
                              int delta_softplus, const float* h0, void* out, float* h_last, bool conv,
                              const float* conv_w, const float* conv_b, cudaStream_t s, selscan::FwdParams* p,
-                             bool* done) {
+                             bool* done, float* ckpt = nullptr) {
   *done = false;
   selscan::t_launches = 0;
   if (conv && !conv_w) return SELSCAN_ERR_NULL;
@@ -170,10 +170,13 @@ selscan_status_t prepare_fwd(const selscan_shape_t* shape, const void* u, const 
                       {conv ? conv_w : nullptr, Dm * 16}, {conv ? conv_b : nullptr, Dm * 4}};
   const bool req_in[] = {true, true, true, true, true, false, false, false, false, conv, false};
   const size_t el_in[] = {ei, ei, 4, ei, ei, 4, ei, 4, 4, 4, 4};
-  const Span outs[] = {{out, elems * (int64_t)eo}, {h_last, states * 4}};
-  const bool req_out[] = {true, false};
-  const size_t el_out[] = {eo, 4};
-  st = check_args(ins, req_in, el_in, 11, outs, req_out, el_out, 2, h0, h_last);
+  const int64_t nck = (L + 15) / 16;  // 16-step checkpoint chunks
+  int64_t ck_floats;
+  if (!mul_ok(rows, nck * 16, &ck_floats) || ck_floats > INT64_MAX / 4) return SELSCAN_ERR_SHAPE;
+  const Span outs[] = {{out, elems * (int64_t)eo}, {h_last, states * 4}, {ckpt, ck_floats * 4}};
+  const bool req_out[] = {true, false, false};
+  const size_t el_out[] = {eo, 4, 16};
+  st = check_args(ins, req_in, el_in, 11, outs, req_out, el_out, 3, h0, h_last);
   if (st != SELSCAN_OK) return st;
   if (rows == 0) {
     *done = true;
@@ -215,6 +218,8 @@ selscan_status_t prepare_fwd(const selscan_shape_t* shape, const void* u, const 
   p->conv_w = conv ? conv_w : nullptr;
   p->conv_b = conv ? conv_b : nullptr;
   p->out_bf16 = shape->out_dtype == SELSCAN_BF16;
+  p->ckpt = ckpt;
+  p->ckpt_chunks = nck;
   return SELSCAN_OK;
 }
 
@@ -328,14 +333,18 @@ size_t selscan_bwd_workspace_size(const selscan_shape_t* shape) {
   return selscan::bwd_workspace_bytes(shape->batch, shape->dim, shape->seqlen);
 }
 
-// The backward: the checks of the forward's inputs plus dout, dh_last and the gradient outputs, zeroing
-// of the accumulated gradients, then one kernel.
-selscan_status_t selscan_bwd(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
-                             const void* B, const void* C, const float* D, const void* z,
-                             const float* delta_bias, int delta_softplus, const float* h0, const void* dout,
-                             const float* dh_last, void* du, void* ddelta, void* dz, float* dA, float* dB,
-                             float* dC, float* dD, float* ddelta_bias, float* dh0, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward: the checks of the forward's inputs plus dout, dh_last, the checkpoints (optional) and the
+// gradient outputs, zeroing of the accumulated gradients, then its kernels.
+selscan_status_t bwd_impl(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                          const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                          int delta_softplus, const float* h0, const void* dout, const float* dh_last,
+                          const float* ckpt, void* du, void* ddelta, void* dz, float* dA, float* dB, float* dC,
+                          float* dD, float* ddelta_bias, float* dh0, void* workspace, size_t workspace_bytes,
+                          void* stream) {
   selscan::t_launches = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   selscan_status_t st = check_shape(shape);
@@ -350,21 +359,22 @@ selscan_status_t selscan_bwd(const selscan_shape_t* shape, const void* u, const 
   if (elems > INT64_MAX / 16 || bc_elems > INT64_MAX / 4 || states > INT64_MAX / 4) return SELSCAN_ERR_SHAPE;
   if (Bsz > 65535) return SELSCAN_ERR_UNSUPPORTED;  // one grid row per batch entry
   const size_t ei = dsize(shape->in_dtype), eo = dsize(shape->out_dtype);
-  const size_t ws_need = selscan::bwd_workspace_bytes(Bsz, Dm, L);
+  const size_t ws_need = selscan::bwd_workspace_bytes(Bsz, Dm, L, ckpt == nullptr);
   if (workspace && workspace_bytes < ws_need) return SELSCAN_ERR_SCRATCH;
+  const int64_t ck_floats = rows * ((L + 15) / 16) * 16;
   const Span ins[] = {{u, elems * (int64_t)ei},    {delta, elems * (int64_t)ei}, {A, an * 4},
                       {B, bc_elems * (int64_t)ei}, {C, bc_elems * (int64_t)ei},  {D, Dm * 4},
                       {z, elems * (int64_t)ei},    {delta_bias, Dm * 4},         {h0, states * 4},
-                      {dout, elems * (int64_t)eo}, {dh_last, states * 4}};
-  const bool req_in[] = {true, true, true, true, true, false, false, false, false, true, false};
-  const size_t el_in[] = {ei, ei, 4, ei, ei, 4, ei, 4, 4, eo, 4};
+                      {dout, elems * (int64_t)eo}, {dh_last, states * 4},        {ckpt, ck_floats * 4}};
+  const bool req_in[] = {true, true, true, true, true, false, false, false, false, true, false, false};
+  const size_t el_in[] = {ei, ei, 4, ei, ei, 4, ei, 4, 4, eo, 4, 16};
   const Span outs[] = {{du, elems * (int64_t)ei}, {ddelta, elems * (int64_t)ei}, {dz, elems * (int64_t)ei},
                        {dA, an * 4},              {dB, bc_elems * 4},             {dC, bc_elems * 4},
                        {dD, Dm * 4},              {ddelta_bias, Dm * 4},          {dh0, states * 4},
                        {workspace, (int64_t)ws_need}};
   const bool req_out[] = {true, true, false, true, true, true, false, false, false, false};
   const size_t el_out[] = {ei, ei, ei, 4, 4, 4, 4, 4, 4, 16};
-  st = check_args(ins, req_in, el_in, 11, outs, req_out, el_out, 10, nullptr, nullptr);
+  st = check_args(ins, req_in, el_in, 12, outs, req_out, el_out, 10, nullptr, nullptr);
   if (st != SELSCAN_OK) return st;
   // The accumulated gradients start from zero (stream-ordered fills, no allocation).
   cudaError_t e = cudaSuccess;
@@ -410,12 +420,57 @@ selscan_status_t selscan_bwd(const selscan_shape_t* shape, const void* u, const 
   p.dD = dD;
   p.ddelta_bias = ddelta_bias;
   p.dh0 = dh0;
+  p.ckpt_in = ckpt;
   p.delta_softplus = delta_softplus != 0;
   p.vec_in = aligned(u, 4 * ei) && aligned(delta, 4 * ei) && (!z || aligned(z, 4 * ei)) && L % 4 == 0;
   p.vec_dout = aligned(dout, 4 * eo) && L % 4 == 0;
   p.vec_grad = aligned(du, 4 * ei) && aligned(ddelta, 4 * ei) && (!dz || aligned(dz, 4 * ei)) && L % 4 == 0;
   p.vec_dbc = aligned(dB, 16) && aligned(dC, 16) && L % 4 == 0;
   e = selscan::launch_bwd(p, shape->in_dtype, shape->out_dtype, workspace, s);
+  return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+selscan_status_t selscan_bwd(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* delta_bias, int delta_softplus, const float* h0, const void* dout,
+                             const float* dh_last, void* du, void* ddelta, void* dz, float* dA, float* dB,
+                             float* dC, float* dD, float* ddelta_bias, float* dh0, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return bwd_impl(shape, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, dout, dh_last, nullptr, du, ddelta,
+                  dz, dA, dB, dC, dD, ddelta_bias, dh0, workspace, workspace_bytes, stream);
+}
+
+// selscan_bwd from the checkpoints selscan_fwd_ckpt kept (the backward's own forward pass is skipped).
+selscan_status_t selscan_bwd_ckpt(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* D, const void* z,
+                                  const float* delta_bias, int delta_softplus, const float* h0, const void* dout,
+                                  const float* dh_last, const float* ckpt, void* du, void* ddelta, void* dz,
+                                  float* dA, float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ckpt && shape && shape->batch > 0 && shape->dim > 0 && shape->seqlen > 0) return SELSCAN_ERR_NULL;
+  return bwd_impl(shape, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, dout, dh_last, ckpt, du, ddelta,
+                  dz, dA, dB, dC, dD, ddelta_bias, dh0, workspace, workspace_bytes, stream);
+}
+
+// The forward that also keeps the state before every 16-step chunk for the backward (selscan_bwd_ckpt).
+selscan_status_t selscan_fwd_ckpt(const selscan_shape_t* shape, const void* u, const void* delta, const float* A,
+                                  const void* B, const void* C, const float* D, const void* z,
+                                  const float* delta_bias, int delta_softplus, const float* h0, void* out,
+                                  float* h_last, float* ckpt, void* stream) {
+  if (!ckpt && shape && shape->batch > 0 && shape->dim > 0 && shape->seqlen > 0) return SELSCAN_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  selscan::FwdParams p;
+  bool done = false;
+  selscan_status_t st = prepare_fwd(shape, u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, out, h_last,
+                                    false, nullptr, nullptr, s, &p, &done, ckpt);
+  if (st != SELSCAN_OK || done) return st;
+  if (!selscan::rows_kernel_supports(p, shape->in_dtype)) return SELSCAN_ERR_UNSUPPORTED;
+  const cudaError_t e = selscan::launch_fwd_rows(p, shape->in_dtype, shape->out_dtype, selscan::RowsOptions{}, s,
+                                                 nullptr);
   return e == cudaSuccess ? SELSCAN_OK : cuda_fail(e);
 }
 

@@ -225,9 +225,11 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
     }
   }
   float4* ck = reinterpret_cast<float4*>(p.ckpt) + grow * nchunks * (kNS / 4) + q;
+  // The checkpoints phase 2 reruns chunks from: the forward's (phase 1 skipped), or phase 1's.
+  const float4* ckr = p.ckpt_in ? reinterpret_cast<const float4*>(p.ckpt_in) + grow * nchunks * (kNS / 4) + q : ck;
 
   // ---- phase 1: the forward, keeping the state at the start of every chunk --------------------------
-  {
+  if (!p.ckpt_in) {
     BCStage<Tin, 1> bs;
     bs.load(p, b, cb);
     const int64_t o0 = static_cast<int64_t>(cb) * kBT;
@@ -313,7 +315,12 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
     bs.store(sm);
     // (Rows past D have no checkpoints: channel 0's belong to its own row.  Their dout is 0, so every
     // contribution they make is 0 whatever their states are.)
-    const float4 c4 = row_ok ? ck[static_cast<int64_t>(c) * (kNS / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 c4 = row_ok ? ckr[static_cast<int64_t>(c) * (kNS / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    // (A forward with fewer than 16 states leaves the slots of states >= N unwritten.)
+    if (4 * q + 0 >= N) c4.x = 0.f;
+    if (4 * q + 1 >= N) c4.y = 0.f;
+    if (4 * q + 2 >= N) c4.z = 0.f;
+    if (4 * q + 3 >= N) c4.w = 0.f;
     float2 hc[2] = {f2(c4.x, c4.y), f2(c4.z, c4.w)};
     // This lane's steps: Δ, Δu, σ(x), dy and the factor of y in dz (zero past the chunk).
     float dlq[4], duq[4], sgq[4], dyq[4], fzq[4], uqv[4];
@@ -688,9 +695,9 @@ cudaError_t launch_typed(const BwdParams& p, cudaStream_t s) {
 
 }  // namespace
 
-size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen) {
+size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, bool with_ckpt) {
   const size_t rows = static_cast<size_t>(batch) * static_cast<size_t>(dim);
-  size_t floats = rows * static_cast<size_t>((seqlen + kBT - 1) / kBT) * kNS;  // checkpoints
+  size_t floats = with_ckpt ? rows * static_cast<size_t>((seqlen + kBT - 1) / kBT) * kNS : 0;  // checkpoints
   const BwdPlan pl = plan_bwd(batch, dim, seqlen);
   if (pl.nblocks > 1) {
     const size_t nb = static_cast<size_t>(pl.nblocks);
@@ -702,9 +709,11 @@ size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen) {
 cudaError_t launch_bwd(const BwdParams& p_in, selscan_dtype_t in_dtype, selscan_dtype_t dout_dtype, void* workspace,
                        cudaStream_t s) {
   BwdParams p = p_in;
+  const bool own_ckpt = p.ckpt_in == nullptr;
+  const size_t ws_bytes = bwd_workspace_bytes(p.batch, p.dim, p.seqlen, own_ckpt);
   void* own = nullptr;
-  if (!workspace) {
-    const cudaError_t e = cudaMallocAsync(&own, bwd_workspace_bytes(p.batch, p.dim, p.seqlen), s);
+  if (!workspace && ws_bytes > 0) {
+    const cudaError_t e = cudaMallocAsync(&own, ws_bytes, s);
     if (e != cudaSuccess) return e;
     workspace = own;
   }
@@ -712,9 +721,10 @@ cudaError_t launch_bwd(const BwdParams& p_in, selscan_dtype_t in_dtype, selscan_
   const size_t rows = static_cast<size_t>(p.batch * p.dim), nb = static_cast<size_t>(pl.nblocks);
   p.nblocks = pl.nblocks;
   p.tblock = pl.tblock;
-  p.ckpt = static_cast<float*>(workspace);
+  float* base = static_cast<float*>(workspace);
+  p.ckpt = own_ckpt ? base : nullptr;
   if (pl.nblocks > 1) {
-    p.summ = p.ckpt + rows * static_cast<size_t>((p.seqlen + kBT - 1) / kBT) * kNS;
+    p.summ = base + (own_ckpt ? rows * static_cast<size_t>((p.seqlen + kBT - 1) / kBT) * kNS : 0);
     p.sumd = p.summ + nb * rows * 2 * kNS;
     p.hstart = p.sumd + align_floats(nb * rows);
     p.gend = p.hstart + nb * rows * kNS;

@@ -48,6 +48,10 @@ struct FwdParams {
   int warps;
   int stages;
   int out_bf16;
+  // Checkpoints (selscan_fwd_ckpt; nullable): the state before every 16-step chunk,
+  // [rows][ckpt_chunks][16] fp32, written by the forward scan for the backward to rerun chunks from.
+  float* ckpt;
+  int64_t ckpt_chunks;
 };
 
 // Arguments of one selscan_step launch.
@@ -95,7 +99,8 @@ struct BwdParams {
   float* dD;           // nullable
   float* ddelta_bias;  // nullable
   float* dh0;          // nullable
-  float* ckpt;         // workspace: the state at the start of every chunk, [rows][chunks][16]
+  float* ckpt;         // the state at the start of every chunk, [rows][chunks][16]: in the workspace, or
+  const float* ckpt_in;  // the forward's (selscan_fwd_ckpt; nullable), in which case phase 1 is skipped
   // Time blocks (nblocks > 1): blocks of tblock steps (a multiple of the chunk), their summaries
   // (zero-start end state and zero-end start gradient, [nblocks][rows][32]; ΣΔ, [nblocks][rows]) and
   // the carried start state and end gradient of every block ([nblocks][rows][16] each).
@@ -113,7 +118,7 @@ struct BwdParams {
 };
 // Bytes of the backward's workspace (chunk checkpoints, and the time blocks' summaries and carries when
 // the problem has too few rows to fill the current device).
-size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen);
+size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, bool with_ckpt = true);
 // The backward: zeroing of the accumulated gradients is the caller's; `workspace` (nullable: taken from
 // the stream's memory pool) holds at least bwd_workspace_bytes.
 cudaError_t launch_bwd(const BwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t dout_dtype, void* workspace,

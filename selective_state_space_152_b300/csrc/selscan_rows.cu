@@ -383,6 +383,17 @@ __device__ __forceinline__ void conv_front(float (&xv)[NV], float x3, float x2, 
 
 // ---- the kernel -----------------------------------------------------------------------------------
 
+// The lane's states before step t, if t starts a 16-step checkpoint chunk inside the sequence and the
+// call keeps checkpoints (selscan_fwd_ckpt): [row][t / 16][n0, n0 + SPL).
+template <int SPL>
+__device__ __forceinline__ void save_ckpt(const FwdParams& p, const float2 (&h)[SPL / 2], int64_t grow, int64_t t,
+                                          bool row_ok, int n0) {
+  if (!p.ckpt || !row_ok || t >= p.seqlen) return;
+  float4* dst = reinterpret_cast<float4*>(p.ckpt + (grow * p.ckpt_chunks + t / 16) * 16 + n0);
+#pragma unroll
+  for (int k = 0; k < SPL / 4; k++) dst[k] = make_float4(h[2 * k].x, h[2 * k].y, h[2 * k + 1].x, h[2 * k + 1].y);
+}
+
 template <int NS, int SPL, typename Tin, bool SUMMARY, bool REV, bool ZOH, bool CONV>
 __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     selscan_fwd_rows_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
@@ -712,6 +723,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         for (int pi = 0; pi < kSB / 2; pi++) {
           const int pr = REV ? kSB / 2 - 1 - pi : pi;
           const int i = 2 * pr;
+          if (!SUMMARY && !REV && i % 16 == 0) save_ckpt<SPL>(p, h, grow, t0 + sb * kSB + i, row_ok, n0);
           float2 ne[SPL], na0[SPL / 2], na1[SPL / 2];
           if (pi + 1 < kSB / 2) {
             const int j = REV ? i - 2 : i + 2;
@@ -785,6 +797,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
             u1 = __shfl_sync(kFull, ru[k + 1], src);
           }
         }
+        if (!SUMMARY && !REV && (2 * gp) % 16 == 0) save_ckpt<SPL>(p, h, grow, t0 + 2 * gp, row_ok, n0);
         update_pair<SPL, TS, REV, ZOH, SUMMARY>(h, IA, eq[g], a0q[g], a1q[g], f2(rq[g].z, rq[g].z),
                                                 f2(rq[g].w, rq[g].w), f2(u0, u0), f2(u1, u1), tB + 2 * gp * TS,
                                                 tC + 2 * gp * TS, yp[tt], yp[tt + 1]);

@@ -161,7 +161,7 @@ def decode_as_sequences(inp, rows):
 GRAD_TOL = {"f32": (1e-4, 1e-4), "bf16": (1e-3, 4e-3)}
 
 
-def gpu_bwd(inp, cot, delta_softplus=True, workspace=None, want_dh0=True):
+def gpu_bwd(inp, cot, delta_softplus=True, workspace=None, want_dh0=True, ckpt=None):
     """selscan_bwd on an input dict and a cotangent dict; float64 numpy gradients keyed like
     oracle.selscan_bwd."""
     import torch
@@ -173,7 +173,7 @@ def gpu_bwd(inp, cot, delta_softplus=True, workspace=None, want_dh0=True):
     gh = to_dev(cot.get("dh_last"))
     g = ss.selscan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], go, D=t["D"], z=t["z"],
                        delta_bias=t["delta_bias"], delta_softplus=delta_softplus, h0=t["h0"], dh_last=gh,
-                       workspace=workspace, want_dh0=want_dh0)
+                       workspace=workspace, want_dh0=want_dh0, ckpt=ckpt)
     torch.cuda.synchronize()
     return {k: (None if v is None else v.float().cpu().numpy().astype(np.float64)) for k, v in g.items()}
 

@@ -177,3 +177,82 @@ def test_bwd_workload_full(name):
     go, gh = oracle_cotangent(cot)
     ref = oracle.selscan_bwd(inp, go, gh)
     check_grads(got, ref, w.in_dtype, what=name)
+
+
+def _truncated(inp, steps):
+    """The input dict cut to its first `steps` steps (the forward oracle's state after them is h_last)."""
+    out = dict(inp)
+    for k in ("u", "delta", "z", "B", "C"):
+        if out.get(k) is not None:
+            out[k] = np.ascontiguousarray(out[k][..., :steps])
+    B, Dm, _, N = inp["shape"]
+    out["shape"] = (B, Dm, steps, N)
+    return out
+
+
+# (batch, dim, seqlen, dstate, in_dtype, forward time blocks)
+CKPT_CASES = [(2, 40, 200, 16, "bf16", None), (1, 24, 100, 16, "f32", "3"), (2, 33, 96, 4, "f32", None),
+              (1, 20, 136, 8, "bf16", "2")]
+
+
+@pytest.mark.parametrize("i", range(len(CKPT_CASES)))
+def test_fwd_ckpt_keeps_the_oracle_states(i, monkeypatch):
+    """selscan_fwd_ckpt's checkpoint c is the state after the first 16·c steps (the oracle's h_last of the
+    sequence cut there), in one pass and in forced time blocks; its out and h_last are selscan_fwd's."""
+    import torch
+
+    import selective_state_space_152_b300 as ss
+    from gpu_util import check_h, check_out
+
+    B, Dm, L, N, dt, tb = CKPT_CASES[i]
+    if tb:
+        monkeypatch.setenv("SELSCAN_TBLOCKS", tb)
+    inp = si.random_case(800 + i, B, Dm, L, N, in_dtype=dt)
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    out, hl, ck = ss.selscan_fwd_ckpt(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                                      delta_bias=t["delta_bias"], h0=t["h0"], return_h_last=True)
+    torch.cuda.synchronize()
+    assert ck.shape == (B, Dm, (L + 15) // 16, 16)
+    ref, href = oracle.selscan_fwd(inp)
+    check_out(out.cpu().numpy().astype(np.float64), ref, dt, what="fwd_ckpt out")
+    check_h(hl.cpu().numpy().astype(np.float64), href, what="fwd_ckpt h_last")
+    ckh = ck.cpu().numpy().astype(np.float64)
+    assert np.array_equal(ckh[:, :, 0, :N], inp["h0"].astype(np.float64))  # before step 0: h0 itself
+    for c in sorted({1, (L // 16) // 2, (L - 1) // 16}):
+        if c < 1:
+            continue
+        _, hc = oracle.selscan_fwd(_truncated(inp, 16 * c))
+        check_h(ckh[:, :, c, :N], hc, what=f"checkpoint {c}")
+
+
+@pytest.mark.parametrize("bwd_blocks", ["1", "3"])
+@pytest.mark.parametrize("i", range(len(CKPT_CASES)))
+def test_bwd_from_forward_checkpoints(i, bwd_blocks, monkeypatch):
+    """selscan_bwd_ckpt from selscan_fwd_ckpt's checkpoints gives every gradient of the oracle, in one
+    time block and in three (the carries then run without the backward's own forward pass)."""
+    import selective_state_space_152_b300 as ss
+
+    B, Dm, L, N, dt, tb = CKPT_CASES[i]
+    if tb:
+        monkeypatch.setenv("SELSCAN_TBLOCKS", tb)
+    monkeypatch.setenv("SELSCAN_BWD_TBLOCKS", bwd_blocks)
+    inp = si.random_case(820 + i, B, Dm, L, N, in_dtype=dt)
+    cot = si.random_cotangents(840 + i, B, Dm, L, N, dout_dtype=dt)
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    _, _, ck = ss.selscan_fwd_ckpt(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                                   delta_bias=t["delta_bias"], h0=t["h0"])
+    got = gpu_bwd(inp, cot, ckpt=ck)
+    go, gh = oracle_cotangent(cot)
+    ref = oracle.selscan_bwd(inp, go, gh)
+    check_grads(got, ref, dt, what=f"bwd from checkpoints {CKPT_CASES[i][:5]}")
+
+
+def test_fwd_ckpt_needs_staged_rows():
+    """Rows the tensor copies cannot stage (L not a multiple of 8 in bf16) are refused: no checkpoints."""
+    import selective_state_space_152_b300 as ss
+
+    inp = si.random_case(850, 1, 8, 37, 16, in_dtype="bf16")
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    with pytest.raises(ss.SelscanError) as e:
+        ss.selscan_fwd_ckpt(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"], delta_bias=t["delta_bias"])
+    assert e.value.status == 4  # SELSCAN_ERR_UNSUPPORTED
