@@ -109,6 +109,11 @@ constexpr int kSB = SELSCAN_ROWS_SB;  // steps per sub-block (16 or 32)
 #define SELSCAN_ROWS_AHEAD 2
 #endif
 // Pause of the producer warp between polls of its two events, in nanoseconds.
+// Q > 1: the record of a step pair is read this many pairs before its exponentials are formed, so the
+// shared-memory latency is not in the way of the exponent multiply.
+#ifndef SELSCAN_ROWS_RECEARLY
+#define SELSCAN_ROWS_RECEARLY 2
+#endif
 #ifndef SELSCAN_ROWS_PSLEEP
 #define SELSCAN_ROWS_PSLEEP 64
 #endif
@@ -294,6 +299,7 @@ __device__ __forceinline__ void update_pair(float2 (&h)[SPL / 2], const float2 (
                                             const float2 (&a0)[SPL / 2], const float2 (&a1)[SPL / 2], float2 du0,
                                             float2 du1, float2 u0, float2 u1, const float* __restrict__ Bt,
                                             const float* __restrict__ Ct, float& y0, float& y1) {
+  float2 yk[2];
 #pragma unroll
   for (int kk = 0; kk < 2; kk++) {
     const int k = REV ? 1 - kk : kk;
@@ -320,10 +326,11 @@ __device__ __forceinline__ void update_pair(float2 (&h)[SPL / 2], const float2 (
         if (!SUMMARY) y2 = fma2s(m ? f2(cc.z, cc.w) : f2(cc.x, cc.y), h[p], y2);
       }
     }
-    if (!SUMMARY) {
-      if (k) y1 = y2.x + y2.y;
-      else y0 = y2.x + y2.y;
-    }
+    yk[k] = y2;
+  }
+  if (!SUMMARY) {
+    y0 = yk[0].x + yk[0].y;
+    y1 = yk[1].x + yk[1].y;
   }
 }
 
@@ -384,21 +391,23 @@ __device__ __forceinline__ void conv_front(float (&xv)[NV], float x3, float x2, 
 
 // ---- the kernel -----------------------------------------------------------------------------------
 
-// The lane's states before step t, if t starts a 16-step checkpoint chunk inside the sequence and the
-// call keeps checkpoints (selscan_fwd_ckpt): [row][t / 16][n0, n0 + SPL).
+// The lane's states before step t, if t starts a 16-step checkpoint chunk inside the sequence, into the
+// checkpoints of selscan_fwd_ckpt: [row][t / 16][n0, n0 + SPL).
 template <int SPL>
 __device__ __forceinline__ void save_ckpt(const FwdParams& p, const float2 (&h)[SPL / 2], int64_t grow, int64_t t,
                                           bool row_ok, int n0) {
-  if (!p.ckpt || !row_ok || t >= p.seqlen) return;
+  if (!row_ok || t >= p.seqlen) return;
   float4* dst = reinterpret_cast<float4*>(p.ckpt + (grow * p.ckpt_chunks + t / 16) * 16 + n0);
 #pragma unroll
   for (int k = 0; k < SPL / 4; k++) dst[k] = make_float4(h[2 * k].x, h[2 * k].y, h[2 * k + 1].x, h[2 * k + 1].y);
 }
 
-template <int NS, int SPL, typename Tin, bool SUMMARY, bool REV, bool ZOH, bool CONV>
+// CKPT: the plain forward scan that also keeps the state before every 16-step chunk (p.ckpt).
+template <int NS, int SPL, typename Tin, bool SUMMARY, bool REV, bool ZOH, bool CONV, bool CKPT = false>
 __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     selscan_fwd_rows_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
   static_assert(!(CONV && REV), "the convolution front is causal: forward direction only");
+  static_assert(!CKPT || (!SUMMARY && !REV && !ZOH && !CONV), "checkpoints of the plain forward scan only");
   using G = RowsGeom<NS, SPL, Tin, ZOH, CONV>;
   constexpr int Q = G::Q, RPW = G::RPW, RB = G::RB, TS = G::TS;
   const int W = p.warps, S = p.stages;
@@ -724,7 +733,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         for (int pi = 0; pi < kSB / 2; pi++) {
           const int pr = REV ? kSB / 2 - 1 - pi : pi;
           const int i = 2 * pr;
-          if (!SUMMARY && !REV && i % 16 == 0) save_ckpt<SPL>(p, h, grow, t0 + sb * kSB + i, row_ok, n0);
+          if (CKPT && i % 16 == 0) save_ckpt<SPL>(p, h, grow, t0 + sb * kSB + i, row_ok, n0);
           float2 ne[SPL], na0[SPL / 2], na1[SPL / 2];
           if (pi + 1 < kSB / 2) {
             const int j = REV ? i - 2 : i + 2;
@@ -775,15 +784,22 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
       // unit's latency overlaps the FMAs of the pairs in between (only AH + 1 pairs are live at a time).
       float4 rq[P];
       float2 eq[P][SPL], a0q[P][SPL / 2], a1q[P][SPL / 2];
+      constexpr int RE = SELSCAN_ROWS_RECEARLY;
+      auto load_rec = [&](int g) { rq[g] = record(REV ? P - 1 - g : g); };
       auto start = [&](int g) {
-        rq[g] = record(REV ? P - 1 - g : g);
+        if (RE == 0) load_rec(g);
         expo_pair<SPL>(f2(rq[g].x, rq[g].y), A2d, eq[g], a0q[g], a1q[g]);
       };
+      if (RE > 0) {
+#pragma unroll
+        for (int g = 0; g < AH + RE && g < P; g++) load_rec(g);
+      }
 #pragma unroll
       for (int g = 0; g < AH && g < P; g++) start(g);
       float yp[kSB];
 #pragma unroll
       for (int g = 0; g < P; g++) {
+        if (RE > 0 && g + AH + RE < P) load_rec(g + AH + RE);
         if (g + AH < P) start(g + AH);
         const int gp = REV ? P - 1 - g : g, sb = gp / PS, tt = 2 * (gp % PS);
         float u0 = 0.f, u1 = 0.f;
@@ -798,7 +814,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
             u1 = __shfl_sync(kFull, ru[k + 1], src);
           }
         }
-        if (!SUMMARY && !REV && (2 * gp) % 16 == 0) save_ckpt<SPL>(p, h, grow, t0 + 2 * gp, row_ok, n0);
+        if (CKPT && (2 * gp) % 16 == 0) save_ckpt<SPL>(p, h, grow, t0 + 2 * gp, row_ok, n0);
         update_pair<SPL, TS, REV, ZOH, SUMMARY>(h, IA, eq[g], a0q[g], a1q[g], f2(rq[g].z, rq[g].z),
                                                 f2(rq[g].w, rq[g].w), f2(u0, u0), f2(u1, u1), tB + 2 * gp * TS,
                                                 tC + 2 * gp * TS, yp[tt], yp[tt + 1]);
@@ -1021,12 +1037,21 @@ DevInfo dev_info() {
   return di;
 }
 
+// The scan kernel of one instantiation: with checkpoints (plain scans only; null for an option) or without.
+template <int NS, int SPL, typename Tin, bool REV, bool ZOH, bool CONV>
+auto scan_kernel(const FwdParams& p) -> decltype(&selscan_fwd_rows_kernel<NS, SPL, Tin, false, REV, ZOH, CONV>) {
+  if (!p.ckpt) return selscan_fwd_rows_kernel<NS, SPL, Tin, false, REV, ZOH, CONV>;
+  if constexpr (!REV && !ZOH && !CONV) return selscan_fwd_rows_kernel<NS, SPL, Tin, false, false, false, false, true>;
+  return nullptr;
+}
+
 // The plan of one instantiation: warps per CTA (within its shared-memory and register limits), pipeline
 // stages and time blocks, with its estimated cost.
 template <int NS, int SPL, typename Tin, bool REV, bool ZOH, bool CONV>
 cudaError_t plan_cfg(const FwdParams& p, RowsPlan* out) {
   using G = RowsGeom<NS, SPL, Tin, ZOH, CONV>;
-  auto scan = selscan_fwd_rows_kernel<NS, SPL, Tin, false, REV, ZOH, CONV>;
+  const auto scan = scan_kernel<NS, SPL, Tin, REV, ZOH, CONV>(p);
+  if (!scan) return cudaErrorInvalidValue;
   const DevInfo di = dev_info();
   // Largest W whose shared memory fits; CTAs per SM for every W (registers, shared memory, warps).
   cudaFuncAttributes fa;
@@ -1060,7 +1085,8 @@ cudaError_t launch_rows_cfg(const FwdParams& p_in, const RowsPlan& plan, cudaStr
                             bool* too_big) {
   using G = RowsGeom<NS, SPL, Tin, ZOH, CONV>;
   FwdParams p = p_in;
-  auto scan = selscan_fwd_rows_kernel<NS, SPL, Tin, false, REV, ZOH, CONV>;
+  const auto scan = scan_kernel<NS, SPL, Tin, REV, ZOH, CONV>(p);
+  if (!scan) return cudaErrorInvalidValue;
   auto summary = selscan_fwd_rows_kernel<NS, SPL, Tin, true, REV, ZOH, CONV>;
   cudaError_t e = cudaSuccess;
   p.warps = plan.warps;
