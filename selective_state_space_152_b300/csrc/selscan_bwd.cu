@@ -19,7 +19,9 @@
 // states [4q, 4q+4) as two float2 pairs (packed fp32x2 arithmetic), lane = 8q + r, so the 8 rows of a
 // warp that read one state group read the same B, C values (shared-memory broadcast).  Lane q also owns
 // steps [4q, 4q+4) of every chunk: it loads their inputs, forms Δ, Δu, σ(x), σ(z) and dy once, hands
-// Δ, Δu and dy to the row's other lanes by shuffles, and stores those steps' du, dδ and dz.  The next
+// Δ, Δu and dy to the row's other lanes (by shuffles in phase 1, as records in shared memory in phase 2),
+// keeps the row sums of its own steps as the sweep passes them, and after the sweep forms and stores
+// those steps' du, dδ and dz, all lanes at once.  The next
 // chunk's inputs are loaded into registers while the current one is computed.  The row's lanes add
 // their partial sums over states (y, Σ G B, Σ A G Ā h) with two shuffles.  dB and dC are sums over the
 // channels of a batch entry: per step a warp adds up its 8 rows' contributions by recursive halving (7
@@ -42,10 +44,17 @@ constexpr int kNS = 16;         // states per row held by the 4 lanes (lanes mas
 constexpr int kThreads = kBW * 32;
 constexpr int kTS = kNS + 4;  // floats per step of the B, C tile: the stagers' column writes spread over banks
 
+// The chunk loops of phase 2 run in groups of kU steps, unrolled within a group and not across groups:
+// fully unrolled 16-step loops hoist enough loads to spill at the 168 registers that three CTAs per SM
+// allow (four CTAs, at 128 registers, and two, at 255, both measured slower).
+constexpr int kU = 4;          // a multiple of 4: a group holds whole step quads
+constexpr int kMinBlocks = 3;  // resident CTAs per SM the registers are sized for
+
 struct BwdSmem {
   float bc[2][kBT][kTS];     // B, C of the chunk, [step][state]
   float h[kBW][kBT][32][4];  // per warp: h_{t-1} of every step of the chunk, per lane
   float red[kBW][kBT][32];   // per warp and step: the 8-row sums of dB, dC (lane 8q + r: value r)
+  float4 rec[kBW][kBT][8];   // per warp, step and row: (Δ, Δu, dy, 0) from the lane that prepared the step
 };
 
 __device__ __forceinline__ float row_sum(float v) {
@@ -182,7 +191,7 @@ __device__ __forceinline__ float from_prep(const float (&v)[4], int i, int r) {
 }
 
 template <typename Tin, typename Tg>
-__global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks) selscan_bwd_kernel(const BwdParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -307,15 +316,16 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
     if (has_z) zq = load_quad(z_row + o, n0, p.vec_in);
     gq = load_quad(go_row + o, n0, p.vec_dout);
   }
+  // (Rows past D have no checkpoints: channel 0's belong to its own row.  Their dout is 0, so every
+  // contribution they make is 0 whatever their states are.)
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c = ce - 1; c >= cb; c--) {
     const int64_t t0 = static_cast<int64_t>(c) * kBT;
     const int len = chunk_len(L, c);
     const int nq = quad_len(len, q);
     __syncthreads();  // the previous chunk's B, C and dB/dC sums have been read
     bs.store(sm);
-    // (Rows past D have no checkpoints: channel 0's belong to its own row.  Their dout is 0, so every
-    // contribution they make is 0 whatever their states are.)
-    float4 c4 = row_ok ? ckr[static_cast<int64_t>(c) * (kNS / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 c4 = row_ok ? ckr[static_cast<int64_t>(c) * (kNS / 4)] : zero4;
     // (A forward with fewer than 16 states leaves the slots of states >= N unwritten.)
     if (4 * q + 0 >= N) c4.x = 0.f;
     if (4 * q + 1 >= N) c4.y = 0.f;
@@ -345,6 +355,10 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
       fzq[m] = fz;
       uqv[m] = uu;
     }
+    // The row's lanes read these steps' Δ, Δu and dy from the records (the previous chunk's readers are
+    // done: the CTA synchronised above).
+#pragma unroll
+    for (int m = 0; m < 4; m++) sm.rec[warp][4 * q + m][r] = make_float4(dlq[m], duq[m], dyq[m], 0.f);
     if (c > cb) {  // the next chunk (in scan order: the previous one in time), in flight during this one
       const int n1 = quad_len(chunk_len(L, c - 1), q);
       const int64_t o = static_cast<int64_t>(c - 1) * kBT;
@@ -358,86 +372,103 @@ __global__ void __launch_bounds__(kThreads, 3) selscan_bwd_kernel(const BwdParam
     // Whole chunks (all but possibly the first) run without per-step bounds checks.
     auto rerun_and_sweep = [&](auto whole) {
       constexpr bool W = decltype(whole)::value;
-      // Rerun the chunk from its checkpoint: h_{t-1} of every step to shared memory, y for dz.
-      float dlv[kBT], duv[kBT], dyv[kBT], dzs[4] = {0.f, 0.f, 0.f, 0.f};
+      // Rerun the chunk from its checkpoint: h_{t-1} of every step to shared memory, y for dz.  The steps
+      // run in quads (qd: the quad, prepared by lane qd of the row; k: the step within it).
+      float yq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int o = 0; o < kBT / kU; o++) {
 #pragma unroll
-      for (int i = 0; i < kBT; i++) {
-        if (!W && i >= len) {
-          dlv[i] = duv[i] = dyv[i] = 0.f;
-          continue;
-        }
-        const float dl = from_prep(dlq, i, r), du = from_prep(duq, i, r);
-        dlv[i] = dl;
-        duv[i] = du;
-        dyv[i] = from_prep(dyq, i, r);
-        *reinterpret_cast<float4*>(sm.h[warp][i][lane]) = make_float4(hc[0].x, hc[0].y, hc[1].x, hc[1].y);
-        const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
-        const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
-        const float2 d2 = f2(dl, dl), du2 = f2(du, du);
-        const float2 e0 = mul2s(d2, A2[0]), e1 = mul2s(d2, A2[1]);
-        const float2 a0 = f2(ex2_approx(e0.x), ex2_approx(e0.y)), a1 = f2(ex2_approx(e1.x), ex2_approx(e1.y));
-        hc[0] = fma2s(a0, hc[0], mul2s(du2, f2(Bv.x, Bv.y)));
-        hc[1] = fma2s(a1, hc[1], mul2s(du2, f2(Bv.z, Bv.w)));
-        if (has_z) {
-          const float2 yp2 = fma2s(f2(Cv.z, Cv.w), hc[1], mul2s(f2(Cv.x, Cv.y), hc[0]));
-          const float y = row_sum(yp2.x + yp2.y);
-          if ((i >> 2) == q) dzs[i & 3] = fmaf(Dd, uqv[i & 3], y) * fzq[i & 3];
+        for (int k = 0; k < kU; k++) {
+          const int i = kU * o + k, qd = i >> 2;
+          if (!W && i >= len) continue;
+          const float4 rc = sm.rec[warp][i][r];
+          const float dl = rc.x, du = rc.y;
+          *reinterpret_cast<float4*>(sm.h[warp][i][lane]) = make_float4(hc[0].x, hc[0].y, hc[1].x, hc[1].y);
+          const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
+          const float2 d2 = f2(dl, dl), du2 = f2(du, du);
+          const float2 e0 = mul2s(d2, A2[0]), e1 = mul2s(d2, A2[1]);
+          const float2 a0 = f2(ex2_approx(e0.x), ex2_approx(e0.y)), a1 = f2(ex2_approx(e1.x), ex2_approx(e1.y));
+          hc[0] = fma2s(a0, hc[0], mul2s(du2, f2(Bv.x, Bv.y)));
+          hc[1] = fma2s(a1, hc[1], mul2s(du2, f2(Bv.z, Bv.w)));
+          if (has_z) {
+            const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
+            const float2 yp2 = fma2s(f2(Cv.z, Cv.w), hc[1], mul2s(f2(Cv.x, Cv.y), hc[0]));
+            const float y = row_sum(yp2.x + yp2.y);
+            if (qd == q) yq[k & 3] = y;  // kept by the lane that prepared the step
+          }
         }
       }
-      if (has_z && row_ok && nq > 0) store4(static_cast<Tin*>(p.dz) + grow * L + t0 + 4 * q, nq, p.vec_grad, dzs);
+      if (has_z && row_ok && nq > 0) {
+        float dzs[4];
+#pragma unroll
+        for (int m = 0; m < 4; m++) dzs[m] = fmaf(Dd, uqv[m], yq[m]) * fzq[m];
+        store4(static_cast<Tin*>(p.dz) + grow * L + t0 + 4 * q, nq, p.vec_grad, dzs);
+      }
       __syncwarp();
       // The reverse sweep of the chunk; hn holds h_t (the state after the step being undone).
       float2 hn[2] = {hc[0], hc[1]};
-      float dus[4] = {0.f, 0.f, 0.f, 0.f}, dxs[4] = {0.f, 0.f, 0.f, 0.f};
+      // Σ_n G B and Σ_n A G Ā h of the steps this lane prepared (zero for steps past the chunk).
+      float Sq[4] = {0.f, 0.f, 0.f, 0.f}, Tq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int o = kBT / kU - 1; o >= 0; o--) {
 #pragma unroll
-      for (int i = kBT - 1; i >= 0; i--) {
-        if (!W && i >= len) continue;
-        const float4 hp4 = *reinterpret_cast<const float4*>(sm.h[warp][i][lane]);
-        const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
-        const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
-        const float2 hp[2] = {f2(hp4.x, hp4.y), f2(hp4.z, hp4.w)};
-        const float2 B2[2] = {f2(Bv.x, Bv.y), f2(Bv.z, Bv.w)}, C2[2] = {f2(Cv.x, Cv.y), f2(Cv.z, Cv.w)};
-        const float dl = dlv[i], dy = dyv[i];
-        const float2 d2 = f2(dl, dl), dy2 = f2(dy, dy), du2 = f2(duv[i], duv[i]);
-        float2 sGB = f2(0.f, 0.f), sAGw = f2(0.f, 0.f), vB[2], vC[2];
+        for (int k = kU - 1; k >= 0; k--) {
+          const int i = kU * o + k, qd = i >> 2;
+          if (!W && i >= len) continue;
+          const float4 hp4 = *reinterpret_cast<const float4*>(sm.h[warp][i][lane]);
+          const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[0][i][4 * q]);
+          const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[1][i][4 * q]);
+          const float2 hp[2] = {f2(hp4.x, hp4.y), f2(hp4.z, hp4.w)};
+          const float2 B2[2] = {f2(Bv.x, Bv.y), f2(Bv.z, Bv.w)}, C2[2] = {f2(Cv.x, Cv.y), f2(Cv.z, Cv.w)};
+          const float4 rc = sm.rec[warp][i][r];
+          const float dl = rc.x, du = rc.y, dy = rc.z;
+          const float2 d2 = f2(dl, dl), dy2 = f2(dy, dy), du2 = f2(du, du);
+          float2 sGB = f2(0.f, 0.f), sAGw = f2(0.f, 0.f), vB[2], vC[2];
 #pragma unroll
-        for (int k = 0; k < 2; k++) {
-          const float2 e = mul2s(d2, A2[k]);
-          const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
-          const float2 G = fma2s(dy2, C2[k], g[k]);
-          const float2 t = mul2s(G, mul2s(ab, hp[k]));  // G Ā h_{t-1}
-          vB[k] = mul2s(G, du2);                        // this row's dB
-          vC[k] = mul2s(dy2, hn[k]);                    // this row's dC
-          sGB = fma2s(G, B2[k], sGB);
-          sAGw = fma2s(Ar[k], t, sAGw);
-          dA[k] = fma2s(t, d2, dA[k]);
-          g[k] = mul2s(G, ab);
-          hn[k] = hp[k];
-        }
-        // dB, dC: the sum over the warp's 8 rows by recursive halving; lane 8q + r ends with value r of
-        // {dB of states 4q..4q+3, dC of states 4q..4q+3}.
-        const float v[8] = {vB[0].x, vB[0].y, vB[1].x, vB[1].y, vC[0].x, vC[0].y, vC[1].x, vC[1].y};
-        float w4[4], w2[2];
+          for (int j = 0; j < 2; j++) {
+            const float2 e = mul2s(d2, A2[j]);
+            const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
+            const float2 G = fma2s(dy2, C2[j], g[j]);
+            const float2 t = mul2s(G, mul2s(ab, hp[j]));  // G Ā h_{t-1}
+            vB[j] = mul2s(G, du2);                        // this row's dB
+            vC[j] = mul2s(dy2, hn[j]);                    // this row's dC
+            sGB = fma2s(G, B2[j], sGB);
+            sAGw = fma2s(Ar[j], t, sAGw);
+            dA[j] = fma2s(t, d2, dA[j]);
+            g[j] = mul2s(G, ab);
+            hn[j] = hp[j];
+          }
+          // dB, dC: the sum over the warp's 8 rows by recursive halving; lane 8q + r ends with value r of
+          // {dB of states 4q..4q+3, dC of states 4q..4q+3}.
+          const float v[8] = {vB[0].x, vB[0].y, vB[1].x, vB[1].y, vC[0].x, vC[0].y, vC[1].x, vC[1].y};
+          float w4[4], w2[2];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-          const float send = b2 ? v[j] : v[4 + j];
-          w4[j] = (b2 ? v[4 + j] : v[j]) + __shfl_xor_sync(kFull, send, 4);
-        }
+          for (int j = 0; j < 4; j++) {
+            const float send = b2 ? v[j] : v[4 + j];
+            w4[j] = (b2 ? v[4 + j] : v[j]) + __shfl_xor_sync(kFull, send, 4);
+          }
 #pragma unroll
-        for (int j = 0; j < 2; j++) {
-          const float send = b1 ? w4[j] : w4[2 + j];
-          w2[j] = (b1 ? w4[2 + j] : w4[j]) + __shfl_xor_sync(kFull, send, 2);
+          for (int j = 0; j < 2; j++) {
+            const float send = b1 ? w4[j] : w4[2 + j];
+            w2[j] = (b1 ? w4[2 + j] : w4[j]) + __shfl_xor_sync(kFull, send, 2);
+          }
+          sm.red[warp][i][lane] = (b0 ? w2[1] : w2[0]) + __shfl_xor_sync(kFull, b0 ? w2[0] : w2[1], 1);
+          const float S = row_sum(sGB.x + sGB.y), T = row_sum(sAGw.x + sAGw.y);
+          if (qd == q) {  // kept by the lane that prepared the step
+            Sq[k & 3] = S;
+            Tq[k & 3] = T;
+          }
         }
-        sm.red[warp][i][lane] = (b0 ? w2[1] : w2[0]) + __shfl_xor_sync(kFull, b0 ? w2[0] : w2[1], 1);
-        const float S = row_sum(sGB.x + sGB.y), T = row_sum(sAGw.x + sAGw.y);
-        if ((i >> 2) == q) {  // the lane that prepared this step stores its gradients
-          const int m = i & 3;
-          const float dx = fmaf(uqv[m], S, T) * sgq[m];
-          dus[m] = fmaf(dy, Dd, dl * S);
-          dxs[m] = dx;
-          dD = fmaf(dy, uqv[m], dD);
-          dbias += dx;
-        }
+      }
+      // The gradients of this lane's own steps, all lanes at once.
+      float dus[4], dxs[4];
+#pragma unroll
+      for (int m = 0; m < 4; m++) {
+        const float dx = fmaf(uqv[m], Sq[m], Tq[m]) * sgq[m];
+        dus[m] = fmaf(dyq[m], Dd, dlq[m] * Sq[m]);
+        dxs[m] = dx;
+        dD = fmaf(dyq[m], uqv[m], dD);
+        dbias += dx;
       }
       if (row_ok && nq > 0) {
         store4(static_cast<Tin*>(p.du) + grow * L + t0 + 4 * q, nq, p.vec_grad, dus);
@@ -645,7 +676,7 @@ BwdPlan plan_bwd(int64_t batch, int64_t dim, int64_t L) {
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
     sms = v > 0 ? v : 148;
   }
-  const int64_t ctas = ((dim + kRows - 1) / kRows) * batch, slots = static_cast<int64_t>(sms) * 3;
+  const int64_t ctas = ((dim + kRows - 1) / kRows) * batch, slots = static_cast<int64_t>(sms) * kMinBlocks;
   int64_t nb = 1;
   const char* env = getenv("SELSCAN_BWD_TBLOCKS");
   if (env) {
