@@ -19,7 +19,8 @@
 //   1. (Q > 1) computes Δ = softplus(δ + Δ_bias) and Δ·u once per (row, step) — each of the Q lanes
 //      of a row takes kT/Q of the steps — into a warp-private shared buffer; with Q = 1 each lane does
 //      its own row's steps in registers;
-//   2. walks the kT steps in sub-blocks of kSB, every lane accumulating the partial y of its states;
+//   2. walks the kT steps in sub-blocks of kSB (the whole chunk when Q > 1), every lane accumulating the
+//      partial y of its states;
 //   3. after each sub-block adds the Q partial sums of a row through the warp buffer, each lane taking
 //      kSB/Q of the steps, adds D·u, gates with silu(z) and stores its steps.
 //
@@ -89,11 +90,7 @@ cudaError_t fixed_scratch(float** ptr, size_t* bytes) {
 
 namespace {
 
-constexpr int kT = 32;         // steps per chunk
-#ifndef SELSCAN_ROWS_SB
-#define SELSCAN_ROWS_SB 16
-#endif
-constexpr int kSB = SELSCAN_ROWS_SB;  // steps per sub-block (16 or 32)
+constexpr int kT = 32;  // steps per chunk
 // Q > 1: Δ and Δu reach the Q lanes of a row as one 16-byte record per step pair from a warp buffer (1),
 // or by shuffles from the lane that prepared them (0).
 #ifndef SELSCAN_ROWS_DU_SMEM
@@ -126,16 +123,20 @@ struct RowsGeom {
   static constexpr int RPW = 32 / Q;   // rows per warp
   static constexpr int RB = kT * static_cast<int>(sizeof(Tin));  // bytes of one staged row of a chunk
   static constexpr CUtensorMapSwizzle kSwizzle = RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  static constexpr int NSB = kT / kSB;  // sub-blocks per chunk
-  static constexpr int EPS = kSB / Q;   // steps per lane and sub-block that the lane prepares and stores
+  // Steps per sub-block: with several lanes per row the whole chunk, so that the row's partial sums of y
+  // meet once per chunk (each meeting is a wait on shared memory the warp cannot hide; halving them
+  // measured 3 % faster); with one lane per row, which keeps its inputs of a sub-block in registers, 16.
+  static constexpr int SB = Q == 1 ? 16 : kT;
+  static constexpr int NSB = kT / SB;  // sub-blocks per chunk
+  static constexpr int EPS = SB / Q;   // steps per lane and sub-block that the lane prepares and stores
   static constexpr int TS = NS + 4;     // floats per step of the widened B, C tile
   // Warp-private buffer (Q > 1): per row and step pair the record (Δ_t, Δ_t+1, Δu_t, Δu_t+1), plus with ZOH
   // (u_t, u_t+1); rows padded by 16 bytes so that the 8 rows a quarter-warp reads fall in distinct banks.
   static constexpr int REC = (ZOH ? 6 : 4) * (kT / 2) + 4;  // floats per row
   static constexpr int REC_FLOATS = (Q > 1 && SELSCAN_ROWS_DU_SMEM) ? RPW * REC : 0;
-  // y partials (Q > 1, SELSCAN_ROWS_YRED): [q][row][kSB + 4]; the odd number of 16-byte units per row keeps
+  // y partials (Q > 1, SELSCAN_ROWS_YRED): [q][row][SB + 4]; the odd number of 16-byte units per row keeps
   // the 8 lanes of a quarter-warp in distinct banks both when they write and when they read.
-  static constexpr int YS = kSB + 4;
+  static constexpr int YS = SB + 4;
   static constexpr int Y_FLOATS = (Q > 1 && SELSCAN_ROWS_YRED) ? 32 * YS : 0;
   static constexpr int WARP_FLOATS = REC_FLOATS + Y_FLOATS;
   static_assert(NS % SPL == 0 && SPL % 4 == 0 && (Q == 1 || Q == 2 || Q == 4), "lanes per row");
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
   static_assert(!(CONV && REV), "the convolution front is causal: forward direction only");
   static_assert(!CKPT || (!SUMMARY && !REV && !ZOH && !CONV), "checkpoints of the plain forward scan only");
   using G = RowsGeom<NS, SPL, Tin, ZOH, CONV>;
-  constexpr int Q = G::Q, RPW = G::RPW, RB = G::RB, TS = G::TS;
+  constexpr int Q = G::Q, RPW = G::RPW, RB = G::RB, TS = G::TS, kSB = G::SB;
   const int W = p.warps, S = p.stages;
   const int ROWS = W * RPW;
   const RowsSmem sm = rows_smem<G, Tin, NS>(W, S);
