@@ -225,6 +225,44 @@ def test_fwd_ckpt_keeps_the_oracle_states(i, monkeypatch):
         check_h(ckh[:, :, c, :N], hc, what=f"checkpoint {c}")
 
 
+def _check_fwd_ckpt(inp, dt, chunks, what):
+    """selscan_fwd_ckpt on inp: out and h_last against the oracle, and checkpoint c (c in chunks) against
+    the oracle's state after the first 16·c steps."""
+    import torch
+
+    import selective_state_space_152_b300 as ss
+    from gpu_util import check_h, check_out
+
+    N = inp["shape"][3]
+    t = {k: to_dev(inp.get(k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias", "h0")}
+    out, hl, ck = ss.selscan_fwd_ckpt(t["u"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                                      delta_bias=t["delta_bias"], h0=t["h0"], return_h_last=True)
+    torch.cuda.synchronize()
+    ref, href = oracle.selscan_fwd(inp)
+    check_out(out.cpu().numpy().astype(np.float64), ref, dt, what=f"{what} out")
+    check_h(hl.cpu().numpy().astype(np.float64), href, what=f"{what} h_last")
+    ckh = ck.cpu().numpy().astype(np.float64)
+    for c in chunks:
+        _, hc = oracle.selscan_fwd(_truncated(inp, 16 * c))
+        check_h(ckh[:, :, c, :N], hc, what=f"{what} checkpoint {c}")
+
+
+@pytest.mark.parametrize("spl", ["4", "8"])
+def test_fwd_ckpt_both_lane_geometries(spl, monkeypatch):
+    """The checkpointing forward with four and with eight states per lane (its two 16-state
+    instantiations), over a ragged last chunk and enough rows for several CTAs."""
+    monkeypatch.setenv("SELSCAN_ROWS_SPL", spl)
+    inp = si.random_case(830 + int(spl), 2, 200, 296, 16, in_dtype="bf16")  # 296 = 9·32 + 8: a ragged last chunk
+    _check_fwd_ckpt(inp, "bf16", [1, 9, 18], f"spl {spl}")
+
+
+def test_fwd_ckpt_workload_full():
+    """The checkpointing forward on the full 130M-like layer: every output and the final state against the
+    oracle, and the checkpoints after 16, 1024 and 2032 steps."""
+    w = si.WORKLOADS["mamba130m_layer"]
+    _check_fwd_ckpt(si.make_inputs(w), w.in_dtype, [1, 64, 127], "mamba130m_layer")
+
+
 @pytest.mark.parametrize("bwd_blocks", ["1", "3"])
 @pytest.mark.parametrize("i", range(len(CKPT_CASES)))
 def test_bwd_from_forward_checkpoints(i, bwd_blocks, monkeypatch):
