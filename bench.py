@@ -570,9 +570,36 @@ def run_e2e(args, torch, ss, inp, w, device, stream, flush, dist, world):
     ev1.record(stream)
     torch.cuda.synchronize()
     secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist, device)
+
+    # The host link's bound for the same bytes: the same copies on the same streams with no scan.
+    def copies(k):
+        with torch.cuda.stream(s_in):
+            for n in names:
+                if host[n] is not None:
+                    sets[k][n].copy_(host[n], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            out_h.copy_(outs[k], non_blocking=True)
+            if hls[k] is not None:
+                hl_h.copy_(hls[k], non_blocking=True)
+
+    copies(0)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    s_in.wait_event(c0)
+    s_out.wait_event(c0)
+    for j in range(steps):
+        copies(j % 2)
+    stream.wait_stream(s_out)
+    stream.wait_stream(s_in)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    link = max_over_ranks(c0.elapsed_time(c1) / 1e3, dist, device)
     return {"value": Bsz * Dm * L * steps * world / secs, "unit": "elems/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": secs / steps * 1e3,
-            "gpu_launches": steps, "pipelined": "h2d / scan / d2h on three streams, two buffer sets"}
+            "gpu_launches": steps, "pipelined": "h2d / scan / d2h on three streams, two buffer sets",
+            "link_bound": {"ms_per_step": link / steps * 1e3, "frac": link / secs,
+                           "what": "the same host copies on the same streams without the scan (pinned memory)"}}
 
 
 def run_options(ss, torch, t, out, h_last, stream, flush, work, sms, hbm_gbs, sm_mhz, rates, steps=50):
