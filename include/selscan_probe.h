@@ -56,6 +56,34 @@ selscan_status_t selscan_probe_rate(int unit, double* per_clk_per_sm);
  */
 selscan_status_t selscan_probe_wait_timeout(int64_t polls, int* completed);
 
+/*
+ * The kernels' own arithmetic of the functions they approximate, evaluated on n values, so that a test can
+ * hold each against a float64 evaluation over its input range:
+ *   SELSCAN_FN_EX2          2^x, the special-function unit's ex2.approx.ftz (every Ā = 2^(Δ·A·log2 e));
+ *   SELSCAN_FN_SOFTPLUS     softplus(x) as the forward and decode kernels form Δ ("Mamba架构与SSM模型：
+ *                           高效序列建模技术解析" §2.2);
+ *   SELSCAN_FN_SILU         x·σ(x), the gate ("Mamba状态空间模型深度解析：挑战Transformer的下一代序列建模
+ *                           范式" §3.1);
+ *   SELSCAN_FN_SOFTPLUS_BWD softplus(x) as the backward forms Δ (together with σ(x) from one exponential);
+ *   SELSCAN_FN_SIGMOID      σ(x), the derivative of softplus, as the backward forms it;
+ *   SELSCAN_FN_ZOH          the exact zero-order-hold input factor (exp(Δ·A) − 1)/A at Δ = x and A = x2
+ *                           (u = 1), through the forward's own steps ("Mamba架构与SSM模型：高效序列建模技术
+ *                           解析" §2.1).
+ * x, x2 and y are device pointers to n fp32 values (x2 only for SELSCAN_FN_ZOH, else ignored; NULL allowed).
+ * Asynchronous on `stream`; allocates nothing.  Returns SELSCAN_ERR_UNSUPPORTED (unknown fn),
+ * SELSCAN_ERR_SHAPE (n < 0 or too many blocks), SELSCAN_ERR_NULL or SELSCAN_ERR_CUDA (launch failed).
+ */
+typedef enum {
+  SELSCAN_FN_EX2 = 0,
+  SELSCAN_FN_SOFTPLUS = 1,
+  SELSCAN_FN_SILU = 2,
+  SELSCAN_FN_SOFTPLUS_BWD = 3,
+  SELSCAN_FN_SIGMOID = 4,
+  SELSCAN_FN_ZOH = 5
+} selscan_fn_t;
+
+selscan_status_t selscan_probe_function(int fn, const float* x, const float* x2, float* y, int64_t n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,9 +24,11 @@ STATUS = {0: "SELSCAN_OK", 1: "SELSCAN_ERR_NULL", 2: "SELSCAN_ERR_SHAPE", 3: "SE
 EXPORTED = ("selscan_fwd", "selscan_step", "selscan_status_string", "selscan_last_cuda_error", "selscan_device_status",
             "selscan_abi_version", "selscan_fwd_noalloc", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_probe_rate",
             "selscan_last_launch_count", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_probe_wait_timeout",
-            "selscan_fwd_ckpt", "selscan_bwd_ckpt")
+            "selscan_fwd_ckpt", "selscan_bwd_ckpt", "selscan_probe_function")
 # Units of selscan_probe_rate (include/selscan_probe.h).
 PROBE_UNITS = {"ex2": 0, "lg2": 1, "rcp": 2, "tanh": 3, "ffma": 4, "ffma2": 5}
+# Functions of selscan_probe_function (include/selscan_probe.h).
+PROBE_FUNCTIONS = {"ex2": 0, "softplus": 1, "silu": 2, "softplus_bwd": 3, "sigmoid": 4, "zoh": 5}
 SELSCAN_FLAG_REVERSE, SELSCAN_FLAG_ZOH = 1, 2
 
 
@@ -92,6 +94,8 @@ def load_library(path: Optional[str] = None):
     lib.selscan_probe_wait_timeout.restype = i32
     lib.selscan_probe_rate.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
     lib.selscan_probe_rate.restype = i32
+    lib.selscan_probe_function.argtypes = [i32, vp, vp, vp, ctypes.c_int64, vp]
+    lib.selscan_probe_function.restype = i32
     if path is None:
         _lib = lib
     return lib
@@ -128,6 +132,23 @@ def selscan_probe_rate(unit: str) -> float:
     r = ctypes.c_double(0.0)
     _check(load_library().selscan_probe_rate(PROBE_UNITS[unit], ctypes.byref(r)))
     return r.value
+
+
+def selscan_probe_function(fn: str, x, x2=None, stream=None):
+    """The kernels' own evaluation of one function (``PROBE_FUNCTIONS``) on a contiguous fp32 CUDA tensor
+    ``x`` (``x2``: A for "zoh", same shape); returns a new fp32 tensor (see include/selscan_probe.h)."""
+    import torch
+
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
+        raise SelscanError("x must be a contiguous float32 CUDA tensor")
+    if x2 is not None and not (isinstance(x2, torch.Tensor) and x2.is_cuda and x2.dtype == torch.float32
+                               and x2.is_contiguous() and x2.shape == x.shape):
+        raise SelscanError("x2 must be a contiguous float32 CUDA tensor shaped like x")
+    y = torch.empty_like(x)
+    _check(load_library().selscan_probe_function(PROBE_FUNCTIONS[fn], x.data_ptr(),
+                                                 None if x2 is None else x2.data_ptr(), y.data_ptr(), x.numel(),
+                                                 _stream_handle(stream)))
+    return y
 
 
 def selscan_probe_wait_timeout(polls: int = 4096) -> int:
@@ -438,4 +459,4 @@ def selscan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, delta_
 __all__ = ["selscan_fwd", "selscan_fwd_ckpt", "selscan_bwd", "selscan_bwd_workspace_size", "selscan_probe_wait_timeout", "selscan_fwd_ex", "selscan_fwd_conv", "selscan_fwd_noalloc", "selscan_step",
            "selscan_status_string", "selscan_abi_version", "selscan_last_cuda_error", "selscan_device_status",
            "selscan_probe_rate", "selscan_last_launch_count", "SelscanError", "SelscanShape", "load_library", "LIB_PATH", "EXPORTED",
-           "PROBE_UNITS"]
+           "PROBE_UNITS", "PROBE_FUNCTIONS", "selscan_probe_function"]

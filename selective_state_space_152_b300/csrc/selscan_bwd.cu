@@ -68,16 +68,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
-// softplus(x) and its derivative σ(x) from one exponential: with e = exp(-|x|), softplus = max(x, 0) +
-// log(1 + e) (as softplus_fast evaluates it) and σ(x) = 1/(1 + e) for x ≥ 0, e/(1 + e) for x < 0.
-__device__ __forceinline__ void softplus_sigmoid(float x, float& sp, float& sg) {
-  const float e = ex2_approx(-fabsf(x) * kLog2e);
-  const float big = lg2_approx(1.f + e) * kLn2;
-  const float small = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.33333334f), -0.5f), 1.f);
-  sp = fmaxf(x, 0.f) + (e >= 0.0625f ? big : small);
-  sg = (x >= 0.f ? 1.f : e) * rcp_approx(1.f + e);
-}
-
 // The raw bits of a lane's four steps of one row: 8 bytes of bf16 or 16 bytes of fp32.
 template <typename T>
 struct Quad {

@@ -270,6 +270,32 @@ __device__ __forceinline__ float2 fma2s(float2 a, float2 b, float2 c) { return _
 __device__ __forceinline__ float2 mul2s(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 add2s(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
+// softplus(x) and its derivative σ(x) from one exponential: with e = exp(-|x|), softplus = max(x, 0) +
+// log(1 + e) (as softplus_fast evaluates it) and σ(x) = 1/(1 + e) for x ≥ 0, e/(1 + e) for x < 0.
+__device__ __forceinline__ void softplus_sigmoid(float x, float& sp, float& sg) {
+  const float e = ex2_approx(-fabsf(x) * kLog2e);
+  const float big = lg2_approx(1.f + e) * kLn2;
+  const float small = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.33333334f), -0.5f), 1.f);
+  sp = fmaxf(x, 0.f) + (e >= 0.0625f ? big : small);
+  sg = (x >= 0.f ? 1.f : e) * rcp_approx(1.f + e);
+}
+
+// The input factor of a state pair at one step: Δu (B̄ = Δ·B), or with ZOH u·(Ā - 1)/A where
+// |ΔA| >= 1/16 and Δu·φ(ΔA) below, φ(x) = (e^x - 1)/x = 1 + x/2 + x²/6 + x³/24 + ... truncated after x³
+// (error below x⁴/120 < 1.3e-7 relative there, where Ā - 1 would lose its leading digits; at A = 0 it
+// gives Δu, the limit).  The series is evaluated in the exponent e = x·log2 e itself, its coefficients
+// scaled by powers of ln 2.  e: Δ·A·log2 e of the pair; a: its Ā; uia: u·(1/A) of the pair.
+__device__ __forceinline__ float2 zoh_factor2(float2 du, float2 e, float2 a, float2 uia) {
+  constexpr float c1 = kLn2 / 2.f, c2 = kLn2 * kLn2 / 6.f, c3 = kLn2 * kLn2 * kLn2 / 24.f;
+  constexpr float kSmall = 0.0625f / kLn2;  // |ΔA| < 1/16 in units of e
+  float2 phi = fma2s(e, f2(c3, c3), f2(c2, c2));
+  phi = fma2s(e, phi, f2(c1, c1));
+  phi = fma2s(e, phi, f2(1.f, 1.f));
+  const float2 small = mul2s(du, phi);
+  const float2 big = mul2s(add2s(a, f2(-1.f, -1.f)), uia);
+  return f2(fabsf(e.x) < kSmall ? small.x : big.x, fabsf(e.y) < kSmall ? small.y : big.y);
+}
+
 // ---- raw lane segments: the 2H inputs of one lane, as 16-byte vectors per half -------------------
 // Elements are unpacked with shifts and masks on 32-bit words (a bf16 is the top half of an fp32),
 // never through a local array, so everything stays in registers.

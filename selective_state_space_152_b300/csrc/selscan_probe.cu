@@ -84,8 +84,56 @@ cudaError_t run_probe(int sms, long long* cycles, float* sink) {
   return cudaGetLastError();
 }
 
+// y[i] = the kernels' own evaluation of function fn at x[i] (x2[i]: A for SELSCAN_FN_ZOH).
+__global__ void __launch_bounds__(256) fn_kernel(int fn, const float* __restrict__ x, const float* __restrict__ x2,
+                                                 float* __restrict__ y, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float v = x[i];
+  float r = 0.f;
+  switch (fn) {
+    case SELSCAN_FN_EX2: r = ex2_approx(v); break;
+    case SELSCAN_FN_SOFTPLUS: r = softplus_fast(v); break;
+    case SELSCAN_FN_SILU: r = silu_fast(v); break;
+    case SELSCAN_FN_SOFTPLUS_BWD: {
+      float sp, sg;
+      softplus_sigmoid(v, sp, sg);
+      r = sp;
+      break;
+    }
+    case SELSCAN_FN_SIGMOID: {
+      float sp, sg;
+      softplus_sigmoid(v, sp, sg);
+      r = sg;
+      break;
+    }
+    default: {  // SELSCAN_FN_ZOH: the forward's steps for a state with A = x2[i] at Δ = x[i] and u = 1
+      const float a2 = x2[i] * kLog2e;   // A·log2 e, as the kernel keeps it
+      const float e = v * a2;            // the exponent Δ·A·log2 e
+      const float ab = ex2_approx(e);    // Ā
+      const float ia = kLog2e / a2;      // 1/A, as the kernel forms it
+      r = zoh_factor2(f2(v, v), f2(e, e), f2(ab, ab), f2(ia, ia)).x;
+      break;
+    }
+  }
+  y[i] = r;
+}
+
 }  // namespace
 }  // namespace selscan
+
+// The kernels' own arithmetic of one function on n device values: see include/selscan_probe.h.
+extern "C" selscan_status_t selscan_probe_function(int fn, const float* x, const float* x2, float* y, int64_t n,
+                                                   void* stream) {
+  if (fn < SELSCAN_FN_EX2 || fn > SELSCAN_FN_ZOH) return SELSCAN_ERR_UNSUPPORTED;
+  if (n < 0) return SELSCAN_ERR_SHAPE;
+  if (n == 0) return SELSCAN_OK;
+  if (!x || !y || (fn == SELSCAN_FN_ZOH && !x2)) return SELSCAN_ERR_NULL;
+  const int64_t blocks = (n + 255) / 256;
+  if (blocks > 0x7fffffff) return SELSCAN_ERR_SHAPE;
+  selscan::fn_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(fn, x, x2, y, n);
+  return cudaGetLastError() == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
+}
 
 extern "C" selscan_status_t selscan_probe_rate(int unit, double* per_clk_per_sm) {
   using namespace selscan;

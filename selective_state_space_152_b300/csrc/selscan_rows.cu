@@ -259,22 +259,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// The input factor of a state pair at one step: Δu (B̄ = Δ·B), or with ZOH u·(Ā - 1)/A where
-// |ΔA| >= 1/16 and Δu·φ(ΔA) below, φ(x) = (e^x - 1)/x = 1 + x/2 + x²/6 + x³/24 + ... truncated after x³
-// (error below x⁴/120 < 1.3e-7 relative there, where Ā - 1 would lose its leading digits; at A = 0 it
-// gives Δu, the limit).  The series is evaluated in the exponent e = x·log2 e itself, its coefficients
-// scaled by powers of ln 2.  e: Δ·A·log2 e of the pair; a: its Ā; uia: u·(1/A) of the pair.
-__device__ __forceinline__ float2 zoh_factor2(float2 du, float2 e, float2 a, float2 uia) {
-  constexpr float c1 = kLn2 / 2.f, c2 = kLn2 * kLn2 / 6.f, c3 = kLn2 * kLn2 * kLn2 / 24.f;
-  constexpr float kSmall = 0.0625f / kLn2;  // |ΔA| < 1/16 in units of e
-  float2 phi = fma2s(e, f2(c3, c3), f2(c2, c2));
-  phi = fma2s(e, phi, f2(c1, c1));
-  phi = fma2s(e, phi, f2(1.f, 1.f));
-  const float2 small = mul2s(du, phi);
-  const float2 big = mul2s(add2s(a, f2(-1.f, -1.f)), uia);
-  return f2(fabsf(e.x) < kSmall ? small.x : big.x, fabsf(e.y) < kSmall ? small.y : big.y);
-}
-
 // The exponentials of two consecutive steps (i, i+1) of one lane's SPL states: the exponent is formed for
 // both steps at once per state, e_n = (Δ_i, Δ_i+1)·(A_n, A_n)·log2 e, and each 2^e is written straight
 // into the (state 2p, state 2p+1) pair of its step, the operand layout of the packed state update.
