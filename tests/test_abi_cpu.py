@@ -133,3 +133,21 @@ def test_binding_rejects_cpu_tensors():
     with pytest.raises((ValueError, RuntimeError)):
         ss.selscan_fwd(u, u, torch.zeros(2, 1), torch.zeros(1, 1, 4), torch.zeros(1, 1, 4),
                        out=torch.zeros(1, 2, 4), stream=0)
+
+
+def test_probe_function_checks_its_arguments(lib):
+    # (fn, x, x2, y, n): every case fails before the library touches the GPU
+    assert lib.selscan_probe_function(6, FAKE, FAKE, FAKE, 4, None) == 4  # unknown function: UNSUPPORTED
+    assert lib.selscan_probe_function(-1, FAKE, FAKE, FAKE, 4, None) == 4
+    assert lib.selscan_probe_function(0, FAKE, None, FAKE, -1, None) == 2  # n < 0: SHAPE
+    assert lib.selscan_probe_function(0, None, None, FAKE, 4, None) == 1  # no x: NULL
+    assert lib.selscan_probe_function(2, FAKE, None, None, 4, None) == 1  # no y: NULL
+    assert lib.selscan_probe_function(5, FAKE, None, FAKE, 4, None) == 1  # ZOH without A: NULL
+    assert lib.selscan_probe_function(0, None, None, None, 0, None) == 0  # nothing to do: OK, no launch
+
+
+def test_probe_wait_timeout_checks_its_arguments(lib):
+    c = ctypes.c_int(-1)
+    assert lib.selscan_probe_wait_timeout(4, None) == 1
+    assert lib.selscan_probe_wait_timeout(0, ctypes.byref(c)) == 2
+    assert lib.selscan_probe_wait_timeout((1 << 20) + 1, ctypes.byref(c)) == 2
