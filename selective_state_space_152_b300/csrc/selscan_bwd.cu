@@ -472,8 +472,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) selscan_bwd_kernel(const
     __syncthreads();
     // dB, dC of the chunk: the CTA's warps added up, then one atomic add per (tensor, state, 4 steps).
     {
-      const int j = threadIdx.x;  // 128 threads: tensor (1 bit), state (4 bits), step quad (2 bits)
-      const int tensor = j >> 6, n = (j >> 2) & 15, s4 = j & 3;
+      // 128 threads: warp = step quad, lane = (tensor, state), so the 32 lanes of a warp read 32 different
+      // banks of the warps' sums (lane 8q + r of a warp's sums lies in bank 8q + r).
+      const int j = threadIdx.x;
+      const int s4 = j >> 5, tensor = (j >> 4) & 1, n = j & 15;
       const int src = (n >> 2) * 8 + tensor * 4 + (n & 3);
       const int steps = quad_len(len, s4);
       if (n < N && steps > 0) {
