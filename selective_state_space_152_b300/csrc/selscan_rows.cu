@@ -105,12 +105,12 @@ constexpr int kT = 32;  // steps per chunk
 #ifndef SELSCAN_ROWS_AHEAD
 #define SELSCAN_ROWS_AHEAD 2
 #endif
-// Pause of the producer warp between polls of its two events, in nanoseconds.
 // Q > 1: the record of a step pair is read this many pairs before its exponentials are formed, so the
 // shared-memory latency is not in the way of the exponent multiply.
 #ifndef SELSCAN_ROWS_RECEARLY
 #define SELSCAN_ROWS_RECEARLY 2
 #endif
+// Pause of the producer warp between polls of its two events, in nanoseconds.
 #ifndef SELSCAN_ROWS_PSLEEP
 #define SELSCAN_ROWS_PSLEEP 64
 #endif
