@@ -223,9 +223,11 @@ selscan_status_t selscan_fwd_noalloc(const selscan_shape_t* shape, const void* u
  *   dD[d] = Σ_{b,t} dy_t · u_t,   dΔ_bias[d] = Σ_{b,t} dδ_t,   dh0 = g after t = 0
  *
  * (σ is the logistic function, the derivative of softplus; with delta_softplus == 0, dδ_t = dΔ_t.)
- * The forward's states are not stored: the kernel recomputes them, keeping only the state at the start
+ * The forward's states are not stored: the call recomputes them, keeping only the state at the start
  * of every 16-step chunk in `workspace` — the recomputation that "Mamba状态空间模型深度解析：挑战
- * Transformer的下一代序列建模范式" §2.2 describes for training.
+ * Transformer的下一代序列建模范式" §2.2 describes for training.  Where the forward's row-sequential
+ * kernel can stage the rows (as selscan_fwd_ckpt requires) and needs no time blocks, that kernel forms
+ * the checkpoints in a launch of its own before the backward; otherwise the backward kernel does.
  *
  *   u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0 : the forward call's inputs (as selscan_fwd)
  *   dout        : [B, D, L]  out_dtype   ∂loss/∂out
@@ -311,9 +313,10 @@ int selscan_abi_version(void);
  * The number of kernels that the last selscan_fwd, selscan_fwd_ex, selscan_fwd_conv,
  * selscan_fwd_noalloc, selscan_fwd_ckpt, selscan_bwd, selscan_bwd_ckpt or selscan_step call on this
  * host thread enqueued: 1 for a forward or backward run in one pass or a decode step, 3 for a forward
- * or backward run in time blocks (the summary pass, the carry pass and the scan), 0 when the call
- * enqueued no kernel (an argument error, no rows, or an empty sequence, whose state is passed on by a
- * copy).
+ * or backward run in time blocks (the summary pass, the carry pass and the scan), one more for a
+ * selscan_bwd whose checkpoints come from a forward launch of their own (see selscan_bwd), 0 when the
+ * call enqueued no kernel (an argument error, no rows, or an empty sequence, whose state is passed on
+ * by a copy).
  * The pages have no counterpart; it lets a caller (or a benchmark) account for the
  * launches of its timed region.
  */

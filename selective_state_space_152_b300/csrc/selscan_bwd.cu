@@ -29,7 +29,9 @@
 // 4q..4q+3}), the CTA adds its warps in shared memory at the end of the chunk, and one 16-byte atomic add
 // per (tensor, state, 4 steps) goes to global memory.  dA, dD and dΔ_bias are summed in registers over
 // the sequence and added with one atomic per row and value.
+#include <cstdint>
 #include <cstdlib>
+#include <cstring>
 #include <type_traits>
 
 #include "selscan_internal.cuh"
@@ -752,12 +754,45 @@ cudaError_t launch_bwd(const BwdParams& p_in, selscan_dtype_t in_dtype, selscan_
     p.hstart = p.sumd + align_floats(nb * rows);
     p.gend = p.hstart + nb * rows * kNS;
   }
-  cudaError_t e;
-  if (in_dtype == SELSCAN_F32)
-    e = dout_dtype == SELSCAN_F32 ? launch_typed<float, float>(p, s) : launch_typed<float, __nv_bfloat16>(p, s);
-  else
-    e = dout_dtype == SELSCAN_F32 ? launch_typed<__nv_bfloat16, float>(p, s)
-                                  : launch_typed<__nv_bfloat16, __nv_bfloat16>(p, s);
+  cudaError_t e = cudaSuccess;
+  if (own_ckpt) {
+    // The forward pass by the row-sequential kernel, checkpoints only, where it needs no time blocks: then
+    // the backward reruns its chunks from those checkpoints and skips its own phase 1.
+    FwdParams f;
+    memset(&f, 0, sizeof f);
+    const int64_t vin = in_dtype == SELSCAN_F32 ? 4 : 8;  // elements per 16 bytes
+    auto a16 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+    f.batch = p.batch;
+    f.dim = p.dim;
+    f.seqlen = p.seqlen;
+    f.dstate = p.dstate;
+    f.u = p.u;
+    f.delta = p.delta;
+    f.B = p.B;
+    f.C = p.C;
+    f.A = p.A;
+    f.delta_bias = p.delta_bias;
+    f.h0 = p.h0;
+    f.delta_softplus = p.delta_softplus;
+    f.vec_in = a16(p.u) && a16(p.delta) && p.seqlen % vin == 0;
+    f.vec_bc = a16(p.B) && a16(p.C) && p.seqlen % vin == 0;
+    f.vec_stage = f.vec_in && f.vec_bc;
+    f.tblock = p.seqlen;
+    f.nblocks = 1;
+    f.ckpt = p.ckpt;
+    f.ckpt_chunks = (p.seqlen + kBT - 1) / kBT;
+    f.ckpt_only = 1;
+    bool launched = false;
+    e = launch_ckpt_pass(f, in_dtype, s, &launched);
+    if (e == cudaSuccess && launched) p.ckpt_in = p.ckpt;
+  }
+  if (e == cudaSuccess) {
+    if (in_dtype == SELSCAN_F32)
+      e = dout_dtype == SELSCAN_F32 ? launch_typed<float, float>(p, s) : launch_typed<float, __nv_bfloat16>(p, s);
+    else
+      e = dout_dtype == SELSCAN_F32 ? launch_typed<__nv_bfloat16, float>(p, s)
+                                    : launch_typed<__nv_bfloat16, __nv_bfloat16>(p, s);
+  }
   if (own) {
     const cudaError_t ef = cudaFreeAsync(own, s);
     if (e == cudaSuccess) e = ef;

@@ -52,6 +52,8 @@ struct FwdParams {
   // [rows][ckpt_chunks][16] fp32, written by the forward scan for the backward to rerun chunks from.
   float* ckpt;
   int64_t ckpt_chunks;
+  // With ckpt: keep only the checkpoints (no out, h_last or gate): the backward's forward pass.
+  int ckpt_only;
 };
 
 // Arguments of one selscan_step launch.
@@ -191,6 +193,10 @@ bool rows_kernel_supports(const FwdParams& p, selscan_dtype_t in_dtype);
 // *too_big and enqueues nothing when the time blocks need more than the fixed array holds.
 cudaError_t launch_fwd_rows(const FwdParams& p, selscan_dtype_t in_dtype, selscan_dtype_t out_dtype,
                             const RowsOptions& o, cudaStream_t s, bool* too_big);
+// The backward's forward pass by the row-sequential kernel: only the checkpoints p.ckpt (p.ckpt_only set),
+// in one pass over the sequence.  *launched is false, with nothing enqueued, when the rows cannot be staged
+// by tensor copies or would need time blocks; the caller then forms the checkpoints itself.
+cudaError_t launch_ckpt_pass(const FwdParams& p, selscan_dtype_t in_dtype, cudaStream_t s, bool* launched);
 
 // ---------------------------------------------------------------------------------------------
 // Device helpers

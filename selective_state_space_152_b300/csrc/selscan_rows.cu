@@ -387,12 +387,14 @@ __device__ __forceinline__ void save_ckpt(const FwdParams& p, const float2 (&h)[
   for (int k = 0; k < SPL / 4; k++) dst[k] = make_float4(h[2 * k].x, h[2 * k].y, h[2 * k + 1].x, h[2 * k + 1].y);
 }
 
-// CKPT: the plain forward scan that also keeps the state before every 16-step chunk (p.ckpt).
+// CKPT: the plain forward scan that also keeps the state before every 16-step chunk (p.ckpt); with
+// SUMMARY as well, the checkpoint pass: from the start state, keeping only the checkpoints (no C, y or
+// outputs), the forward pass a backward reruns its chunks from.
 template <int NS, int SPL, typename Tin, bool SUMMARY, bool REV, bool ZOH, bool CONV, bool CKPT = false>
 __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     selscan_fwd_rows_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
   static_assert(!(CONV && REV), "the convolution front is causal: forward direction only");
-  static_assert(!CKPT || (!SUMMARY && !REV && !ZOH && !CONV), "checkpoints of the plain forward scan only");
+  static_assert(!CKPT || (!REV && !ZOH && !CONV), "checkpoints of the plain forward scan only");
   using G = RowsGeom<NS, SPL, Tin, ZOH, CONV>;
   constexpr int Q = G::Q, RPW = G::RPW, RB = G::RB, TS = G::TS, kSB = G::SB;
   const int W = p.warps, S = p.stages;
@@ -571,7 +573,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
 #pragma unroll
     for (int k = 0; k < 2; k++) {
       const int n = n0 + 2 * i + k;
-      if (SUMMARY || n >= N || !row_ok)
+      if ((SUMMARY && !CKPT) || n >= N || !row_ok)
         hh[k] = 0.f;
       else if (p.nblocks > 1)
         hh[k] = p.start[(static_cast<int64_t>(kblk) * rows_total + grow) * N + n];
@@ -870,6 +872,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
   }
   if (!ok) return;
 
+  if (SUMMARY && CKPT) return;  // the checkpoint pass keeps nothing else
   if (SUMMARY) {
     // Each prep lane summed Δ over its slice of the block's steps; the row's Q lanes add them up.
 #pragma unroll
@@ -1026,7 +1029,10 @@ DevInfo dev_info() {
 template <int NS, int SPL, typename Tin, bool REV, bool ZOH, bool CONV>
 auto scan_kernel(const FwdParams& p) -> decltype(&selscan_fwd_rows_kernel<NS, SPL, Tin, false, REV, ZOH, CONV>) {
   if (!p.ckpt) return selscan_fwd_rows_kernel<NS, SPL, Tin, false, REV, ZOH, CONV>;
-  if constexpr (!REV && !ZOH && !CONV) return selscan_fwd_rows_kernel<NS, SPL, Tin, false, false, false, false, true>;
+  if constexpr (!REV && !ZOH && !CONV) {
+    if (p.ckpt_only) return selscan_fwd_rows_kernel<NS, SPL, Tin, true, false, false, false, true>;
+    return selscan_fwd_rows_kernel<NS, SPL, Tin, false, false, false, false, true>;
+  }
   return nullptr;
 }
 
@@ -1220,6 +1226,47 @@ cudaError_t launch_fwd_rows(const FwdParams& p_in, selscan_dtype_t in_dtype, sel
                                           : dispatch_rows_opts<__nv_bfloat16>(p, o, s, &tb);
   if (too_big) *too_big = tb;
   return e;
+}
+
+namespace {
+
+// The checkpoint pass with the plan the forward would take (two or four lanes per row by cost), when
+// that plan needs no time blocks.
+template <int NS, typename Tin>
+cudaError_t ckpt_pass_ns(const FwdParams& p, cudaStream_t s, bool* launched) {
+  RowsPlan p4;
+  cudaError_t e = plan_cfg<NS, 4, Tin, false, false, false>(p, &p4);
+  if (e != cudaSuccess) return e;
+  if constexpr (NS >= 8) {
+    RowsPlan p8;
+    e = plan_cfg<NS, 8, Tin, false, false, false>(p, &p8);
+    if (e != cudaSuccess) return e;
+    if (p8.cost < p4.cost) {
+      if (p8.nblocks > 1) return cudaSuccess;
+      e = launch_rows_cfg<NS, 8, Tin, false, false, false>(p, p8, s, ScratchSource::Pool, nullptr);
+      *launched = e == cudaSuccess;
+      return e;
+    }
+  }
+  if (p4.nblocks > 1) return cudaSuccess;
+  e = launch_rows_cfg<NS, 4, Tin, false, false, false>(p, p4, s, ScratchSource::Pool, nullptr);
+  *launched = e == cudaSuccess;
+  return e;
+}
+
+template <typename Tin>
+cudaError_t ckpt_pass(const FwdParams& p, cudaStream_t s, bool* launched) {
+  if (p.dstate <= 4) return ckpt_pass_ns<4, Tin>(p, s, launched);
+  if (p.dstate <= 8) return ckpt_pass_ns<8, Tin>(p, s, launched);
+  return ckpt_pass_ns<16, Tin>(p, s, launched);
+}
+
+}  // namespace
+
+cudaError_t launch_ckpt_pass(const FwdParams& p, selscan_dtype_t in_dtype, cudaStream_t s, bool* launched) {
+  *launched = false;
+  if (!p.ckpt || !p.ckpt_only || !rows_kernel_supports(p, in_dtype)) return cudaSuccess;
+  return in_dtype == SELSCAN_F32 ? ckpt_pass<float>(p, s, launched) : ckpt_pass<__nv_bfloat16>(p, s, launched);
 }
 
 namespace {

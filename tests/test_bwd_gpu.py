@@ -154,16 +154,19 @@ def test_bwd_requires_dz_with_z():
 
 
 def test_bwd_launch_count(monkeypatch):
-    """One kernel for one time block; three (summary, carry, block-wise backward) for several."""
+    """The checkpointing forward pass first when the row-sequential kernel can stage the rows in one pass
+    (else the backward forms its checkpoints itself), then one kernel for one time block and three
+    (summary, carry, block-wise backward) for several."""
     import selective_state_space_152_b300 as ss
 
-    inp, cot = _case(44, 1, 32, 64, 16, "f32", "f32", {})
-    monkeypatch.setenv("SELSCAN_BWD_TBLOCKS", "1")
-    gpu_bwd(inp, cot)
-    assert ss.selscan_last_launch_count() == 1
-    monkeypatch.setenv("SELSCAN_BWD_TBLOCKS", "2")
-    gpu_bwd(inp, cot)
-    assert ss.selscan_last_launch_count() == 3
+    inp, cot = _case(44, 1, 32, 64, 16, "f32", "f32", {})  # whole 16-byte rows: the pass applies
+    ragged, rcot = _case(45, 1, 32, 66, 16, "f32", "f32", {})  # 66 fp32 steps: rows the copies cannot stage
+    for blocks, own in (("1", 1), ("2", 3)):
+        monkeypatch.setenv("SELSCAN_BWD_TBLOCKS", blocks)
+        gpu_bwd(inp, cot)
+        assert ss.selscan_last_launch_count() == 1 + own
+        gpu_bwd(ragged, rcot)
+        assert ss.selscan_last_launch_count() == own
 
 
 @pytest.mark.parametrize("name", ["mamba130m_layer", "width_2p8b", "long_seq_65k"])
