@@ -27,6 +27,8 @@ CASES = [
                                     "has_dh_last": False}),  # no optional input
     (2, 48, 300, 16, "f32", "f32", {"softplus": False}),     # Δ = δ + Δ_bias (no softplus)
     (2, 96, 2048, 16, "bf16", "bf16", {}),                   # 128 chunks, three CTAs per batch entry
+    (2, 20, 96, 3, "bf16", "bf16", {}),                      # checkpoints by the one-lane-per-row forward pass
+    (1, 44, 200, 8, "f32", "bf16", {}),                      # checkpoints by the 8-state forward pass
 ]
 
 
