@@ -783,8 +783,13 @@ cudaError_t launch_bwd(const BwdParams& p_in, selscan_dtype_t in_dtype, selscan_
     f.ckpt_chunks = (p.seqlen + kBT - 1) / kBT;
     f.ckpt_only = 1;
     bool launched = false;
-    e = launch_ckpt_pass(f, in_dtype, s, &launched);
-    if (e == cudaSuccess && launched) p.ckpt_in = p.ckpt;
+    if (launch_ckpt_pass(f, in_dtype, s, &launched) == cudaSuccess && launched) {
+      p.ckpt_in = p.ckpt;
+    } else {
+      // The pass could not be set up (nothing of it ran): the backward kernel forms the checkpoints.  An
+      // error that outlives the call (a device fault) is reported by the backward kernel's own launch.
+      (void)cudaGetLastError();
+    }
   }
   if (e == cudaSuccess) {
     if (in_dtype == SELSCAN_F32)
